@@ -1,0 +1,431 @@
+#!/usr/bin/env python3
+"""Benchmark of the Ulysses attention layer on GB300.
+
+One step is the whole hot path on one batch of seeded synthetic input:
+
+  Q, K, V seq->head, attention forward, O head->seq,
+  dO seq->head, attention backward, dQ, dK, dV head->seq
+
+(forward-only workloads stop after O head->seq). The default workload is the
+Llama-8B-shaped forward+backward layer at sl=32768: P=8 virtual ranks, 32 query
+heads, 8 kv heads, head size 128, bf16, causal.
+
+Output: one JSON line on rank 0. ``value`` is tokens/s over the whole job,
+timed with CUDA events with inputs already resident in HBM. ``e2e`` is the
+same metric through the public API, with the host->device copy of the step's
+inputs and the device->host copy of its outputs inside the timed region.
+``--impl reference`` times the CPU oracle instead, on a bounded sample.
+
+Under torchrun (N > 1) every rank runs an independent replica of the layer on
+its own GPU. The path has no exchange between GPUs: all P ranks of one layer
+are virtual shards on one GPU. Rank 0 prints the job line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, doc_offsets_for, make_global_inputs, split_shards  # noqa: E402
+
+METRIC = "attn fwd+bwd tokens/s & TFLOPS (% bf16 peak); exchange GB/s (% HBM) at 1 GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------------------
+# Work accounting (algorithmic, not measured)
+# ---------------------------------------------------------------------------
+def visible_pairs(sl, causal, offs):
+    """Visible (query, key) pairs of one (batch, head): the work the mask leaves."""
+    offs = offs or [0, sl]
+    tot = 0
+    for a, b in zip(offs[:-1], offs[1:]):
+        n = b - a
+        tot += n * (n + 1) // 2 if causal else n * n
+    return tot
+
+
+def attn_flops(w, sl=None, offs=None):
+    """Forward flops: 2 GEMMs (QK^T, PV) of 2*hs flops per visible pair and head."""
+    sl = sl or w.sl
+    offs = offs if offs is not None else doc_offsets_for(w)
+    return 4.0 * w.hs * w.hc * w.bs * visible_pairs(sl, w.causal, offs)
+
+
+def exchange_bytes(w, H):
+    """One exchange reads and writes the whole [sl, bs, H, hs] tensor once."""
+    return 2.0 * w.sl * w.bs * H * w.hs * w.elem_bytes
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# Our implementation
+# ---------------------------------------------------------------------------
+def run_ours(args, w, rank, world):
+    import ulysses_sequence_attention_gb300 as U
+    from ulysses_sequence_attention_gb300 import _binding as B
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    offs = doc_offsets_for(w)
+    x = make_global_inputs(w)
+    P = w.P
+    seq = {k: [t.to(dev) for t in split_shards(v, P)] for k, v in x.items()}
+    L = U.UlyssesLayer(w.sl, w.bs, w.hc, w.hkv, w.hs, P, w.causal, offs, w.torch_dtype, device=str(dev))
+    o = L.new_seq_shards(w.hc)
+    if w.backward:
+        dq, dk, dv = L.new_seq_shards(w.hc), L.new_seq_shards(w.hkv), L.new_seq_shards(w.hkv)
+    L._alloc(backward=w.backward)
+    b = L.head_buffers
+    h = L.h
+    stream = torch.cuda.current_stream(dev)
+    ev = {}
+
+    def mark(name):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        ev.setdefault(name, []).append(e)
+
+    def step(timed):
+        if timed:
+            mark("s2h0")
+        B.ulysses_seq_to_head(h, w.hc, seq["q"], b["qh"])
+        B.ulysses_seq_to_head(h, w.hkv, seq["k"], b["kh"])
+        B.ulysses_seq_to_head(h, w.hkv, seq["v"], b["vh"])
+        if timed:
+            mark("fwd0")
+        B.ulysses_attn_fwd(h, b["qh"], b["kh"], b["vh"], b["oh"], b["lse"])
+        if timed:
+            mark("fwd1")
+        B.ulysses_head_to_seq(h, w.hc, b["oh"], o)
+        if w.backward:
+            B.ulysses_seq_to_head(h, w.hc, seq["do"], b["doh"])
+            if timed:
+                mark("bwd0")
+            B.ulysses_attn_bwd(h, b["qh"], b["kh"], b["vh"], b["oh"], b["doh"], b["lse"],
+                               b["dqh"], b["dkh"], b["dvh"], b["ws"])
+            if timed:
+                mark("bwd1")
+            B.ulysses_head_to_seq(h, w.hc, b["dqh"], dq)
+            B.ulysses_head_to_seq(h, w.hkv, b["dkh"], dk)
+            B.ulysses_head_to_seq(h, w.hkv, b["dvh"], dv)
+        if timed:
+            mark("end")
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize(dev)
+    st = U.ulysses_get_status(h)
+    if st != U.ULYSSES_OK:
+        raise RuntimeError(f"device status after warm-up: {U.ulysses_strerror(st)}")
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    n0 = U.ulysses_launch_count()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(True)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    launches = U.ulysses_launch_count() - n0
+    clk = clocks.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    if U.ulysses_get_status(h) != U.ULYSSES_OK:
+        raise RuntimeError("device status after the timed region is not OK")
+
+    def span(a, z):
+        return [ea.elapsed_time(ez) for ea, ez in zip(ev[a], ev[z])]
+
+    fwd_ms = statistics.mean(span("fwd0", "fwd1"))
+    s2h_ms = statistics.mean(span("s2h0", "fwd0"))
+    bwd_ms = statistics.mean(span("bwd0", "bwd1")) if w.backward else 0.0
+
+    # max over ranks
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    tokens = w.sl * w.bs * args.steps * world
+    value = tokens / (elapsed_ms / 1e3)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, L, x, dev, world, barrier)
+
+    result = {"ms_per_step": ms_per_step, "value": value, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+              "s2h_qkv_ms": s2h_ms, "launches": launches, "clocks": clk, "e2e": e2e}
+    return result
+
+
+def run_e2e(args, w, L, x, dev, world, barrier):
+    """The same metric through UlyssesLayer with host<->device copies in the timed region."""
+    P = w.P
+    pin = {k: [t.pin_memory() for t in split_shards(v, P)] for k, v in x.items()}
+    dseq = {k: [torch.empty_like(t, device=dev) for t in v] for k, v in pin.items()}
+    o = L.new_seq_shards(w.hc)
+    outs = [o]
+    if w.backward:
+        dq, dk, dv = L.new_seq_shards(w.hc), L.new_seq_shards(w.hkv), L.new_seq_shards(w.hkv)
+        outs += [dq, dk, dv]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in grp] for grp in outs]
+    h2d = sum(t.numel() * t.element_size() for v in pin.values() for t in v)
+    d2h = sum(t.numel() * t.element_size() for grp in outs for t in grp)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for k in pin:
+            for src, dst in zip(pin[k], dseq[k]):
+                dst.copy_(src, non_blocking=True)
+        L.forward(dseq["q"], dseq["k"], dseq["v"], o)
+        if w.backward:
+            L.backward(dseq["do"], dq, dk, dv)
+        for grp, hgrp in zip(outs, host_out):
+            for src, dst in zip(grp, hgrp):
+                dst.copy_(src, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms = t0.elapsed_time(t1)
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms = float(t.item())
+    return {"value": w.sl * w.bs * args.steps * world / (ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample(w, sl_sample):
+    """Time the oracle's whole layer (fwd, and bwd if the workload has one) at sl_sample.
+
+    Same P, heads, head size and mask kind as the workload. Returns
+    (seconds, tokens/s scaled to the full workload by visible-pair work).
+    """
+    import oracle
+    from workloads import random_inputs
+    offs = None
+    if w.ndoc:
+        # the same number of documents, scaled down
+        full = doc_offsets_for(w)
+        offs = sorted({round(o * sl_sample / w.sl) for o in full})
+    x = random_inputs(sl_sample, w.bs, w.hc, w.hkv, w.hs, w.torch_dtype, w.seed, with_grad=w.backward)
+    qs, ks, vs = (oracle.shard_sequence(x[n], w.P) for n in ("q", "k", "v"))
+    t0 = time.perf_counter()
+    oracle.ulysses_forward(qs, ks, vs, w.P, causal=w.causal, doc_offsets=offs)
+    if w.backward:
+        oracle.ulysses_backward(qs, ks, vs, oracle.shard_sequence(x["do"], w.P), w.P, causal=w.causal,
+                                doc_offsets=offs)
+    sec = time.perf_counter() - t0
+    work_ratio = attn_flops(w) / attn_flops(w, sl_sample, offs)
+    return sec, w.sl * w.bs / (sec * work_ratio)
+
+
+def cores_used():
+    return torch.get_num_threads()
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return None
+    sl_sample = args.ref_sl
+    for _ in range(args.warmup):
+        oracle_sample(w, sl_sample)
+    secs, vals = [], []
+    for _ in range(args.steps):
+        s, v = oracle_sample(w, sl_sample)
+        secs.append(s)
+        vals.append(v)
+    value = statistics.mean(vals)
+    sample = (f"oracle (torch fp64 CPU) whole layer {'fwd+bwd' if w.backward else 'fwd'} at sl={sl_sample} "
+              f"(same P/heads/hs/mask), tokens/s scaled to sl={w.sl} by visible-pair work")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.mean(secs), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"kind": "oracle", "cores": cores_used(), "sample": sample, "value": value,
+                             "unit": "tokens/s"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def workload_config(w):
+    return {"workload": w.name, "P": w.P, "global_batch": w.bs, "seq_len": w.sl, "hc": w.hc, "hkv": w.hkv,
+            "hs": w.hs, "causal": w.causal, "ndoc": w.ndoc or 1, "backward": w.backward,
+            "parallelism": f"ulysses sp{w.P} (virtual ranks on one GPU)",
+            "l2": "inputs larger than L2 (Q alone %.0f MiB)" % (w.sl * w.bs * w.hc * w.hs * w.elem_bytes / 2**20)}
+
+
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama8b_32k", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sl", type=int, default=4096, help="oracle sample length for cpu_baseline")
+    ap.add_argument("--ref-sl", type=int, default=2048, help="oracle sample length per reference step")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    w = WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    if world > 1:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+
+    r = run_ours(args, w, rank, world)
+    if rank == 0:
+        peaks, src = load_peaks()
+        offs = doc_offsets_for(w)
+        fl_fwd = attn_flops(w, offs=offs)
+        fl_bwd = 2.5 * fl_fwd if w.backward else 0.0
+        fwd_tf = fl_fwd / (r["fwd_ms"] * 1e-3) / 1e12
+        bwd_tf = fl_bwd / (r["bwd_ms"] * 1e-3) / 1e12 if w.backward else None
+        x_bytes = exchange_bytes(w, w.hc) + 2 * exchange_bytes(w, w.hkv)
+        s2h_gbs = x_bytes / (r["s2h_qkv_ms"] * 1e-3) / 1e9
+        sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        if w.backward:
+            dom = {"kernel": "ulysses_attn_bwd", "achieved": bwd_tf, "ms": r["bwd_ms"], "flops": fl_bwd}
+        else:
+            dom = {"kernel": "ulysses_attn_fwd", "achieved": fwd_tf, "ms": r["fwd_ms"], "flops": fl_fwd}
+        roof = {"bound": "tensor", "kernel": dom["kernel"], "achieved": dom["achieved"], "peak": sustained,
+                "unit": "TFLOP/s", "frac": dom["achieved"] / sustained, "traffic": None,
+                "peak_source": f"{src} bf16_tflops_sustained",
+                "frac_of_burst": dom["achieved"] / peaks["bf16_tflops"],
+                "algorithmic_tflop_per_launch": dom["flops"] / 1e12, "avg_launch_ms": dom["ms"]}
+        cpu = None
+        if not args.no_cpu_baseline:
+            sec, val = oracle_sample(w, args.cpu_sl)
+            cpu = {"value": val, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
+                   "sample": (f"oracle (torch fp64 CPU) whole layer {'fwd+bwd' if w.backward else 'fwd'} at "
+                              f"sl={args.cpu_sl} (same P/heads/hs/mask) took {sec:.2f} s; tokens/s scaled to "
+                              f"sl={w.sl} by visible-pair work")}
+        line = {"metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+                "data": "synthetic (seeded N(0,1) Q/K/V/dO of the workload's shape)",
+                "config": workload_config(w),
+                "roofline": roof,
+                "cpu_baseline": cpu,
+                "e2e": r["e2e"],
+                "gpu_launches": r["launches"],
+                "clocks": r["clocks"],
+                "attention": {"fwd_ms": r["fwd_ms"], "fwd_tflops": fwd_tf, "fwd_frac_sustained": fwd_tf / sustained,
+                              "bwd_ms": r["bwd_ms"], "bwd_tflops": bwd_tf,
+                              "bwd_frac_sustained": (bwd_tf / sustained) if bwd_tf else None,
+                              "fwd_tflop": fl_fwd / 1e12, "bwd_tflop": fl_bwd / 1e12},
+                "exchange": {"s2h_qkv_ms": r["s2h_qkv_ms"], "s2h_qkv_gbs": s2h_gbs,
+                             "s2h_qkv_frac_hbm": s2h_gbs / peaks["hbm_gbs"], "hbm_peak_gbs": peaks["hbm_gbs"],
+                             "hbm_peak_source": src},
+                "context": "pages' figure (not a target): ALST trains a 500K-token sequence for Llama-8B on one H100"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,215 @@
+/*
+ * ulysses.h — C ABI of the GB300 Ulysses sequence-parallel attention layer.
+ *
+ * The layer is DeepSpeed-Ulysses as the pages describe it. The HF blog
+ * "Ulysses Sequence Parallelism: Training with Million-Token Contexts" lists
+ * the algorithm steps: sequence sharding, QKV projection, all-to-all, local
+ * attention, all-to-all, output projection. The DeepSpeed-Ulysses blog
+ * ("DeepSpeed Ulysses: 训练极长序列Transformer模型的系统优化", section
+ * "DeepSpeed-Ulysses的核心设计") gives the core design. This library is the
+ * path between the projections:
+ *
+ *   P sequence shards [sl/P, bs, H, hs]
+ *     --seq->head exchange-->  P head shards [sl, bs, H/P, hs]
+ *     --exact causal softmax attention, forward and backward, per head-->
+ *     --head->seq exchange-->  P sequence shards [sl/P, bs, H, hs]
+ *
+ * All P ranks are shard buffers on ONE GPU. An exchange is a permutation
+ * from HBM to HBM, not a collective between GPUs.
+ *
+ * Conventions shared by every call:
+ *  - Layout. Sequence-major HF layout: a sequence shard is [sl/P][bs][H][hs]
+ *    and a head shard is [sl][bs][H/P][hs], row-major (hs fastest). The source
+ *    is the ALST guide ("DeepSpeed Ulysses 序列并行与 Arctic 长序列训练（ALST）集成指南",
+ *    section 1, which fixes the shape [sl, bs, hc, hs]). Rank i holds tokens
+ *    [i*sl/P, (i+1)*sl/P). After seq->head it holds heads [r*H/P, (r+1)*H/P).
+ *    This is the 2-GPU diagram of the Transformers guide, section
+ *    "Ulysses 序列并行的核心原理".
+ *  - GQA. Query head h reads kv head h / (hc/hkv). When P > hkv, rank r holds
+ *    kv head r*hkv/P (replication, ALST guide section 2.1 item (6)).
+ *  - Pointers. Every tensor argument is a HOST array of P DEVICE pointers,
+ *    one per virtual rank. Each pointer must be non-NULL and 16-byte aligned.
+ *    The caller owns every device buffer, including the workspace, and keeps
+ *    it alive until the work queued on the stream has finished.
+ *  - Streams. `stream` is a cudaStream_t (NULL = legacy default stream). Every
+ *    device call only enqueues work on it and returns without synchronising.
+ *    The one exception is ulysses_get_status.
+ *  - Errors. Every int-returning call returns ULYSSES_OK (0) or a negative
+ *    ulysses_status. No C++ exception crosses this boundary. Arguments are
+ *    checked before anything is enqueued. A failed check enqueues nothing.
+ *  - Element types. ULYSSES_BF16 (bfloat16) or ULYSSES_FP32 for
+ *    Q/K/V/O/dO/dQ/dK/dV. The logsumexp is always fp32. Exchanges copy bits;
+ *    they never convert.
+ */
+#ifndef ULYSSES_H
+#define ULYSSES_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque handle. It owns only small metadata (shape, a device copy of the
+ * document offsets, a device status word). Created by ulysses_create, freed by
+ * ulysses_destroy. A handle may be used from one host thread at a time. */
+typedef struct ulysses_layer* ulysses_t;
+
+typedef enum ulysses_status {
+  ULYSSES_OK = 0,
+  ULYSSES_ERR_INVALID_ARG = -1,  /* NULL pointer, bad dtype, malformed document offsets, bad nheads */
+  ULYSSES_ERR_DIVISIBILITY = -2, /* one of the pages' divisibility rules is broken (see ulysses_create) */
+  ULYSSES_ERR_ALIGNMENT = -3,    /* a device pointer is not 16-byte aligned */
+  ULYSSES_ERR_UNSUPPORTED = -4,  /* valid for the method, but outside what this build implements */
+  ULYSSES_ERR_CUDA = -5,         /* a CUDA runtime call failed (allocation, launch) */
+  ULYSSES_ERR_TIMEOUT = -6       /* a device-side bounded wait ran out (reported by ulysses_get_status) */
+} ulysses_status;
+
+typedef enum ulysses_dtype {
+  ULYSSES_BF16 = 0,
+  ULYSSES_FP32 = 1
+} ulysses_dtype;
+
+#define ULYSSES_MAX_P 128
+
+/*
+ * ulysses_create — validate a layer shape and build a handle.
+ *
+ *   sl      global sequence length (all P shards together). 0 is allowed:
+ *           the handle then describes an empty layer and every call is a no-op.
+ *   bs      batch size (0 allowed, as for sl).
+ *   hc      query heads; hkv key/value heads; hs head size (32, 64 or 128).
+ *   P       sequence-parallel degree (virtual ranks), 1 <= P <= ULYSSES_MAX_P.
+ *           P = 1 is legal: the exchanges become plain copies.
+ *   causal  1: key j is visible from query i only when j <= i; 0: all keys
+ *           of the same document are visible.
+ *   doc_offsets  HOST array of ndoc+1 int32 document start offsets in the
+ *           global sequence: [0] = 0, strictly increasing, [ndoc] = sl. Or NULL
+ *           for one document. Position ids restart at each offset, so no key
+ *           is visible across a document boundary. This is the packed-sequence
+ *           rule of the ALST guide, section 2.2. The handle keeps its own copy.
+ *   dtype   ulysses_dtype of the activation tensors.
+ *
+ * Divisibility (ULYSSES_ERR_DIVISIBILITY; ALST guide section 2.1 items (5)
+ * and (6); HF blog section "比较 Ulysses 和 Ring Attention", which requires
+ * num_heads >= sp_size):
+ *   sl % P == 0;  hc % P == 0 (so P <= hc);  hc % hkv == 0;
+ *   hkv % P == 0 or P % hkv == 0.
+ * On any error *out is set to NULL. Allocates a few bytes of device memory on
+ * the current device.
+ */
+int ulysses_create(ulysses_t* out, int64_t sl, int64_t bs, int hc, int hkv, int hs, int P,
+                   int causal, const int32_t* doc_offsets, int ndoc, int dtype);
+
+/* Free the handle and its device metadata. NULL is a no-op. The caller must
+ * make sure that no work using the handle is still running. */
+void ulysses_destroy(ulysses_t h);
+
+/* Static text for a status code. Never NULL. */
+const char* ulysses_strerror(int status);
+
+/*
+ * ulysses_workspace_size — bytes of device workspace that ulysses_attn_bwd needs.
+ * Layout: for each rank, an fp32 dQ accumulator [sl][bs][hc/P][hs], then for
+ * each rank an fp32 D = rowsum(dO * O) array [bs][hc/P][sl]. Pure host
+ * computation.
+ */
+int ulysses_workspace_size(ulysses_t h, size_t* bytes);
+
+/*
+ * ulysses_seq_to_head — the first all-to-all: re-shard from sequence to heads.
+ * HF blog algorithm step 3. Transformers guide: the first all-to-all moves the
+ * sharded dimension from the sequence to the heads.
+ *
+ *   nheads       hc (for Q or dO) or hkv (for K or V).
+ *   seq_shards   P device pointers, each [sl/P][bs][nheads][hs] (input).
+ *   head_shards  P device pointers, each [sl][bs][nheads/P][hs] (output). When
+ *                P > nheads, each is [sl][bs][1][hs] with head r*nheads/P.
+ *   head_shards[r][t][b][j][:] = seq_shards[t/(sl/P)][t%(sl/P)][b][r*nheads/P + j][:]
+ * A bit-exact copy. Input and output buffers must not overlap.
+ */
+int ulysses_seq_to_head(ulysses_t h, int nheads, const void* const* seq_shards,
+                        void* const* head_shards, void* stream);
+
+/*
+ * ulysses_head_to_seq — the second all-to-all: back from heads to sequence.
+ * HF blog algorithm step 5. DeepSpeed-Ulysses blog, section
+ * "DeepSpeed-Ulysses的核心设计": after attention, a second all-to-all turns
+ * the output back into the N/P sequence layout.
+ *
+ *   nheads       hc (O, dQ) or hkv (dK, dV).
+ *   head_shards  P device pointers, each [sl][bs][nheads/P][hs] (input).
+ *   seq_shards   P device pointers, each [sl/P][bs][nheads][hs] (output).
+ * A bit-exact copy when nheads % P == 0. When P > nheads (replicated kv heads),
+ * the input is a gradient. The output for head h is then the sum of the
+ * P/nheads replicas. The sum runs in fp32 and is rounded once to the element
+ * type.
+ */
+int ulysses_head_to_seq(ulysses_t h, int nheads, const void* const* head_shards,
+                        void* const* seq_shards, void* stream);
+
+/*
+ * ulysses_attn_fwd — local exact attention of every rank's head group.
+ * HF blog algorithm step 4 (standard attention per head; heads are
+ * independent). The DeepSpeed-Ulysses blog's per-head equation did not survive
+ * extraction. The equation implemented is the SDPA/FlashAttention definition:
+ *
+ *   S_ij = q_i . k_j / sqrt(hs)
+ *   O_i  = sum_j softmax_j(S_ij over visible j) v_j
+ *   LSE_i = ln sum_{visible j} exp(S_ij)
+ *
+ *   q, o     P pointers, each [sl][bs][hc/P][hs] (head shards)
+ *   k, v     P pointers, each [sl][bs][Hk][hs], Hk = max(hkv/P, 1)
+ *   lse      P pointers, each fp32 [bs][hc/P][sl] (output, kept for backward)
+ * Softmax and the accumulation run in fp32. O is rounded once to the element
+ * type (round to nearest even for bf16).
+ */
+int ulysses_attn_fwd(ulysses_t h, const void* const* q, const void* const* k,
+                     const void* const* v, void* const* o, float* const* lse, void* stream);
+
+/*
+ * ulysses_attn_bwd — gradients of the local attention for L with dL/dO = dO.
+ * The backward of the layer is the reverse of the forward: dO goes through
+ * seq->head, this call runs, and dQ/dK/dV go through head->seq.
+ *
+ *   D_i   = sum_d dO_id O_id
+ *   P_ij  = exp(S_ij - LSE_i)       (visible j; 0 otherwise)
+ *   dV_j  = sum_{q heads of the group} sum_i P_ij dO_i
+ *   dS_ij = P_ij (dO_i . v_j - D_i)
+ *   dQ_i  = sum_j dS_ij k_j / sqrt(hs)
+ *   dK_j  = sum_{q heads of the group} sum_i dS_ij q_i / sqrt(hs)
+ *
+ *   q, o, dO, dq   [sl][bs][hc/P][hs] per rank; k, v, dk, dv [sl][bs][Hk][hs]
+ *   lse            the forward's fp32 [bs][hc/P][sl] per rank
+ *   workspace      device buffer of ulysses_workspace_size bytes, 16-byte
+ *                  aligned, owned by the caller. Its contents on entry are
+ *                  ignored and on exit are unspecified.
+ */
+int ulysses_attn_bwd(ulysses_t h, const void* const* q, const void* const* k,
+                     const void* const* v, const void* const* o, const void* const* dO,
+                     const float* const* lse, void* const* dq, void* const* dk, void* const* dv,
+                     void* workspace, void* stream);
+
+/*
+ * ulysses_get_status — read and clear the handle's device status word.
+ * Synchronises the device. Returns ULYSSES_OK, ULYSSES_ERR_TIMEOUT if a
+ * bounded device-side wait ran out since the last call (the kernel then
+ * returned early and its outputs are invalid), or ULYSSES_ERR_CUDA if the
+ * device reports an error.
+ */
+int ulysses_get_status(ulysses_t h);
+
+/*
+ * ulysses_launch_count — number of CUDA kernels this library has enqueued
+ * since it was loaded, over all handles and threads. A diagnostic counter for
+ * benchmarks: the difference across a region is the number of launches the
+ * region made. Never fails.
+ */
+uint64_t ulysses_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ULYSSES_H */

@@ -10,7 +10,6 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
-    config.addinivalue_line("markers", "slow: long-running CPU oracle work")
 
 
 def pytest_collection_modifyitems(config, items):
@@ -20,6 +19,9 @@ def pytest_collection_modifyitems(config, items):
     except Exception:  # pragma: no cover
         have_gpu = False
     if have_gpu:
+        # The GPU tests load the in-tree library: build it first (a no-op when current).
+        import __graft_entry__
+        __graft_entry__.build()
         return
     skip = pytest.mark.skip(reason="no CUDA GPU in this environment")
     for item in items:

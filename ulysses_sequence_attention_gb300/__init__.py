@@ -1,0 +1,15 @@
+"""GB300-native Ulysses sequence-parallel attention layer.
+
+``_binding`` exposes the C-ABI calls of ``libulysses.so`` under their own names.
+``layer.UlyssesLayer`` strings them together into the layer forward and backward
+for P virtual ranks on one GPU. Importing this package fails loudly when the
+CUDA library has not been built: there is no fallback path.
+"""
+from ._binding import (  # noqa: F401
+    LIB_PATH, ULYSSES_BF16, ULYSSES_ERR_ALIGNMENT, ULYSSES_ERR_CUDA, ULYSSES_ERR_DIVISIBILITY,
+    ULYSSES_ERR_INVALID_ARG, ULYSSES_ERR_TIMEOUT, ULYSSES_ERR_UNSUPPORTED, ULYSSES_FP32,
+    ULYSSES_MAX_P, ULYSSES_OK, UlyssesError, UlyssesHandle, ulysses_attn_bwd, ulysses_attn_fwd,
+    ulysses_create, ulysses_destroy, ulysses_get_status, ulysses_head_to_seq, ulysses_launch_count, ulysses_seq_to_head,
+    ulysses_strerror, ulysses_workspace_size,
+)
+from .layer import UlyssesLayer  # noqa: F401

@@ -1,0 +1,221 @@
+"""ctypes binding of libulysses.so: the C-ABI calls under the same names.
+
+Marshalling only: torch tensors become device pointers, the current torch
+stream becomes a cudaStream_t, and a non-zero status becomes an exception.
+The binding checks each tensor's device, dtype, contiguity and element count
+against the handle's shape before it passes the pointer on, so that a wrong
+buffer fails on the host instead of on the GPU. All compute runs in the
+library's CUDA kernels. There is no fallback: importing this module fails when
+the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libulysses.so")
+
+ULYSSES_OK = 0
+ULYSSES_ERR_INVALID_ARG = -1
+ULYSSES_ERR_DIVISIBILITY = -2
+ULYSSES_ERR_ALIGNMENT = -3
+ULYSSES_ERR_UNSUPPORTED = -4
+ULYSSES_ERR_CUDA = -5
+ULYSSES_ERR_TIMEOUT = -6
+ULYSSES_BF16 = 0
+ULYSSES_FP32 = 1
+ULYSSES_MAX_P = 128
+
+_DTYPES = {"bf16": ULYSSES_BF16, "fp32": ULYSSES_FP32,
+           torch.bfloat16: ULYSSES_BF16, torch.float32: ULYSSES_FP32}
+_TORCH = {ULYSSES_BF16: torch.bfloat16, ULYSSES_FP32: torch.float32}
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with "
+                      "ulysses_sequence_attention_gb300.build.build()")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_vp = ctypes.c_void_p
+_pp = ctypes.POINTER(ctypes.c_void_p)
+lib.ulysses_create.argtypes = [ctypes.POINTER(_vp), ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                               ctypes.POINTER(ctypes.c_int32), ctypes.c_int, ctypes.c_int]
+lib.ulysses_create.restype = ctypes.c_int
+lib.ulysses_destroy.argtypes = [_vp]
+lib.ulysses_destroy.restype = None
+lib.ulysses_strerror.argtypes = [ctypes.c_int]
+lib.ulysses_strerror.restype = ctypes.c_char_p
+lib.ulysses_workspace_size.argtypes = [_vp, ctypes.POINTER(ctypes.c_size_t)]
+lib.ulysses_workspace_size.restype = ctypes.c_int
+lib.ulysses_seq_to_head.argtypes = [_vp, ctypes.c_int, _pp, _pp, _vp]
+lib.ulysses_seq_to_head.restype = ctypes.c_int
+lib.ulysses_head_to_seq.argtypes = [_vp, ctypes.c_int, _pp, _pp, _vp]
+lib.ulysses_head_to_seq.restype = ctypes.c_int
+lib.ulysses_attn_fwd.argtypes = [_vp, _pp, _pp, _pp, _pp, _pp, _vp]
+lib.ulysses_attn_fwd.restype = ctypes.c_int
+lib.ulysses_attn_bwd.argtypes = [_vp] + [_pp] * 9 + [_vp, _vp]
+lib.ulysses_attn_bwd.restype = ctypes.c_int
+lib.ulysses_get_status.argtypes = [_vp]
+lib.ulysses_get_status.restype = ctypes.c_int
+lib.ulysses_launch_count.argtypes = []
+lib.ulysses_launch_count.restype = ctypes.c_uint64
+
+
+class UlyssesError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {ulysses_strerror(status)} ({status})")
+
+
+def ulysses_strerror(status: int) -> str:
+    return lib.ulysses_strerror(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != ULYSSES_OK:
+        raise UlyssesError(status, what)
+
+
+class UlyssesHandle:
+    """Owns one ulysses_t. Shape fields mirror the ulysses_create arguments."""
+
+    def __init__(self, ptr, sl, bs, hc, hkv, hs, P, causal, doc_offsets, dtype):
+        self._ptr = ptr
+        self.sl, self.bs, self.hc, self.hkv, self.hs, self.P = sl, bs, hc, hkv, hs, P
+        self.causal = causal
+        self.doc_offsets = doc_offsets
+        self.dtype = dtype
+        self.Hq = hc // P
+        self.Hk = hkv // P if hkv % P == 0 else 1
+
+    @property
+    def ptr(self):
+        return self._ptr
+
+    @property
+    def torch_dtype(self):
+        return _TORCH[self.dtype]
+
+    def destroy(self):
+        if self._ptr:
+            lib.ulysses_destroy(self._ptr)
+            self._ptr = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def ulysses_create(sl: int, bs: int, hc: int, hkv: int, hs: int, P: int, causal: bool = True,
+                   doc_offsets: Optional[Sequence[int]] = None, dtype="bf16") -> UlyssesHandle:
+    dt = _DTYPES.get(dtype, dtype)
+    out = _vp()
+    if doc_offsets is not None:
+        offs = (ctypes.c_int32 * len(doc_offsets))(*[int(x) for x in doc_offsets])
+        nd = len(doc_offsets) - 1
+    else:
+        offs, nd = None, 0
+    st = lib.ulysses_create(ctypes.byref(out), int(sl), int(bs), int(hc), int(hkv), int(hs), int(P),
+                            int(bool(causal)), offs, nd, int(dt))
+    _check(st, "ulysses_create")
+    return UlyssesHandle(out.value, sl, bs, hc, hkv, hs, P, bool(causal),
+                         None if doc_offsets is None else list(doc_offsets), dt)
+
+
+def ulysses_destroy(h: UlyssesHandle):
+    h.destroy()
+
+
+def ulysses_workspace_size(h: UlyssesHandle) -> int:
+    n = ctypes.c_size_t()
+    _check(lib.ulysses_workspace_size(h.ptr, ctypes.byref(n)), "ulysses_workspace_size")
+    return int(n.value)
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else 0
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptrs(h: UlyssesHandle, tensors, numel: int, dtype: torch.dtype, name: str):
+    if len(tensors) != h.P:
+        raise ValueError(f"{name}: expected {h.P} rank buffers, got {len(tensors)}")
+    out = (_vp * h.P)()
+    for r, t in enumerate(tensors):
+        if isinstance(t, int):
+            out[r] = t
+            continue
+        if t.dtype != dtype:
+            raise TypeError(f"{name}[{r}]: dtype {t.dtype}, expected {dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name}[{r}] must be contiguous")
+        if t.numel() != numel:
+            raise ValueError(f"{name}[{r}]: {t.numel()} elements, expected {numel}")
+        if t.device.type != "cuda":
+            raise ValueError(f"{name}[{r}] must be a CUDA tensor")
+        out[r] = t.data_ptr()
+    return ctypes.cast(out, _pp)
+
+
+def _heads_per_rank(h: UlyssesHandle, nheads: int) -> int:
+    return nheads // h.P if nheads % h.P == 0 else 1
+
+
+def ulysses_seq_to_head(h: UlyssesHandle, nheads: int, seq_shards, head_shards, stream=None):
+    dt = h.torch_dtype
+    n = h.sl // h.P
+    src = _ptrs(h, seq_shards, n * h.bs * nheads * h.hs, dt, "seq_shards")
+    dst = _ptrs(h, head_shards, h.sl * h.bs * _heads_per_rank(h, nheads) * h.hs, dt, "head_shards")
+    _check(lib.ulysses_seq_to_head(h.ptr, int(nheads), src, dst, _stream(stream)), "ulysses_seq_to_head")
+
+
+def ulysses_head_to_seq(h: UlyssesHandle, nheads: int, head_shards, seq_shards, stream=None):
+    dt = h.torch_dtype
+    n = h.sl // h.P
+    src = _ptrs(h, head_shards, h.sl * h.bs * _heads_per_rank(h, nheads) * h.hs, dt, "head_shards")
+    dst = _ptrs(h, seq_shards, n * h.bs * nheads * h.hs, dt, "seq_shards")
+    _check(lib.ulysses_head_to_seq(h.ptr, int(nheads), src, dst, _stream(stream)), "ulysses_head_to_seq")
+
+
+def ulysses_attn_fwd(h: UlyssesHandle, q, k, v, o, lse, stream=None):
+    dt = h.torch_dtype
+    nq = h.sl * h.bs * h.Hq * h.hs
+    nk = h.sl * h.bs * h.Hk * h.hs
+    args = [_ptrs(h, q, nq, dt, "q"), _ptrs(h, k, nk, dt, "k"), _ptrs(h, v, nk, dt, "v"),
+            _ptrs(h, o, nq, dt, "o"), _ptrs(h, lse, h.bs * h.Hq * h.sl, torch.float32, "lse")]
+    _check(lib.ulysses_attn_fwd(h.ptr, *args, _stream(stream)), "ulysses_attn_fwd")
+
+
+def ulysses_attn_bwd(h: UlyssesHandle, q, k, v, o, do, lse, dq, dk, dv, workspace, stream=None):
+    dt = h.torch_dtype
+    nq = h.sl * h.bs * h.Hq * h.hs
+    nk = h.sl * h.bs * h.Hk * h.hs
+    if isinstance(workspace, torch.Tensor):
+        need = ulysses_workspace_size(h)
+        if workspace.device.type != "cuda" or workspace.numel() * workspace.element_size() < need:
+            raise ValueError(f"workspace must be a CUDA buffer of at least {need} bytes")
+        ws = workspace.data_ptr()
+    else:
+        ws = int(workspace)
+    args = [_ptrs(h, q, nq, dt, "q"), _ptrs(h, k, nk, dt, "k"), _ptrs(h, v, nk, dt, "v"),
+            _ptrs(h, o, nq, dt, "o"), _ptrs(h, do, nq, dt, "do"),
+            _ptrs(h, lse, h.bs * h.Hq * h.sl, torch.float32, "lse"),
+            _ptrs(h, dq, nq, dt, "dq"), _ptrs(h, dk, nk, dt, "dk"), _ptrs(h, dv, nk, dt, "dv")]
+    _check(lib.ulysses_attn_bwd(h.ptr, *args, ws, _stream(stream)), "ulysses_attn_bwd")
+
+
+def ulysses_get_status(h: UlyssesHandle) -> int:
+    return int(lib.ulysses_get_status(h.ptr))
+
+
+def ulysses_launch_count() -> int:
+    return int(lib.ulysses_launch_count())

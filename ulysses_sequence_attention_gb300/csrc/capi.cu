@@ -1,0 +1,228 @@
+// capi.cu — the extern "C" boundary: handle life cycle, argument checks, dispatch.
+//
+// Every check in this file runs on the host before anything is enqueued, so a
+// rejected call leaves the device untouched. The divisibility rules come from
+// the ALST guide ("DeepSpeed Ulysses 序列并行与 Arctic 长序列训练（ALST）集成指南",
+// section 2.1, items (5) and (6)). The HF blog ("Ulysses Sequence Parallelism:
+// Training with Million-Token Contexts", section "比较 Ulysses 和 Ring Attention")
+// requires num_heads >= sp_size.
+#include <math.h>
+#include <string.h>
+
+#include <atomic>
+#include <new>
+
+#include "internal.cuh"
+
+namespace uly {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+AttnShape make_shape(const Layer& L) {
+  AttnShape s;
+  s.sl = (int)L.sl;
+  s.bs = (int)L.bs;
+  s.P = L.P;
+  s.Hq = L.Hq;
+  s.Hk = L.Hk;
+  s.group = L.Hq / L.Hk;
+  s.hs = L.hs;
+  s.causal = L.causal;
+  s.ndoc = L.ndoc;
+  s.scale = (float)(1.0 / sqrt((double)L.hs));
+  s.scale_log2 = (float)(1.4426950408889634 / sqrt((double)L.hs));
+  s.doc_offsets = L.d_doc_offsets;
+  s.status = L.d_status;
+  return s;
+}
+
+}  // namespace uly
+
+using uly::Layer;
+
+static int check_ptrs(const void* const* ptrs, int P) {
+  if (!ptrs) return ULYSSES_ERR_INVALID_ARG;
+  for (int r = 0; r < P; ++r) {
+    if (!ptrs[r]) return ULYSSES_ERR_INVALID_ARG;
+    if (((uintptr_t)ptrs[r]) & 15u) return ULYSSES_ERR_ALIGNMENT;
+  }
+  return ULYSSES_OK;
+}
+
+#define CHECK_PTRS(arr)                                             \
+  do {                                                              \
+    int _st = check_ptrs((const void* const*)(arr), L->P);          \
+    if (_st != ULYSSES_OK) return _st;                              \
+  } while (0)
+
+extern "C" {
+
+const char* ulysses_strerror(int status) {
+  switch (status) {
+    case ULYSSES_OK: return "ok";
+    case ULYSSES_ERR_INVALID_ARG: return "invalid argument";
+    case ULYSSES_ERR_DIVISIBILITY: return "divisibility rule broken (sl % P, hc % P, hc % hkv, hkv vs P)";
+    case ULYSSES_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+    case ULYSSES_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ULYSSES_ERR_CUDA: return "CUDA runtime error";
+    case ULYSSES_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int ulysses_create(ulysses_t* out, int64_t sl, int64_t bs, int hc, int hkv, int hs, int P,
+                   int causal, const int32_t* doc_offsets, int ndoc, int dtype) {
+  if (!out) return ULYSSES_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (sl < 0 || bs < 0 || hc <= 0 || hkv <= 0 || hs <= 0 || P <= 0) return ULYSSES_ERR_INVALID_ARG;
+  if (dtype != ULYSSES_BF16 && dtype != ULYSSES_FP32) return ULYSSES_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ULYSSES_ERR_INVALID_ARG;
+  // Divisibility rules of the method.
+  if (hc % P != 0) return ULYSSES_ERR_DIVISIBILITY;
+  if (sl % P != 0) return ULYSSES_ERR_DIVISIBILITY;
+  if (hc % hkv != 0) return ULYSSES_ERR_DIVISIBILITY;
+  if (hkv % P != 0 && P % hkv != 0) return ULYSSES_ERR_DIVISIBILITY;
+  // Limits of this build.
+  if (P > ULYSSES_MAX_P) return ULYSSES_ERR_UNSUPPORTED;
+  if (hs != 32 && hs != 64 && hs != 128) return ULYSSES_ERR_UNSUPPORTED;
+  if (sl > (int64_t(1) << 30) || bs > 65535) return ULYSSES_ERR_UNSUPPORTED;
+  const int64_t esize = dtype == ULYSSES_BF16 ? 2 : 4;
+  if (sl * bs * (int64_t)hc * hs * esize > (int64_t(1) << 38)) return ULYSSES_ERR_UNSUPPORTED;
+  // Document offsets: position ids restart at every offset (ALST guide, section 2.2).
+  if (doc_offsets) {
+    if (ndoc < 1 || doc_offsets[0] != 0 || doc_offsets[ndoc] != sl) return ULYSSES_ERR_INVALID_ARG;
+    for (int d = 0; d < ndoc; ++d)
+      if (doc_offsets[d + 1] <= doc_offsets[d]) return ULYSSES_ERR_INVALID_ARG;
+  } else if (ndoc != 0 && ndoc != 1) {
+    return ULYSSES_ERR_INVALID_ARG;
+  }
+
+  Layer* L = new (std::nothrow) Layer();
+  if (!L) return ULYSSES_ERR_INVALID_ARG;
+  L->sl = sl;
+  L->bs = bs;
+  L->hc = hc;
+  L->hkv = hkv;
+  L->hs = hs;
+  L->P = P;
+  L->causal = causal;
+  L->dtype = dtype;
+  L->Hq = hc / P;
+  L->Hk = hkv % P == 0 ? hkv / P : 1;
+  if (doc_offsets) {
+    L->ndoc = ndoc;
+    L->doc_offsets.assign(doc_offsets, doc_offsets + ndoc + 1);
+  } else {
+    L->ndoc = 1;
+    L->doc_offsets = {0, (int32_t)sl};
+  }
+  if (cudaGetDevice(&L->device) != cudaSuccess) {
+    delete L;
+    return ULYSSES_ERR_CUDA;
+  }
+  cudaError_t e = cudaMalloc(&L->d_status, sizeof(unsigned));
+  if (e == cudaSuccess) e = cudaMemset(L->d_status, 0, sizeof(unsigned));
+  if (e == cudaSuccess) e = cudaMalloc(&L->d_doc_offsets, sizeof(int32_t) * (L->ndoc + 1));
+  if (e == cudaSuccess)
+    e = cudaMemcpy(L->d_doc_offsets, L->doc_offsets.data(), sizeof(int32_t) * (L->ndoc + 1),
+                   cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(L->d_status);
+    cudaFree(L->d_doc_offsets);
+    delete L;
+    return ULYSSES_ERR_CUDA;
+  }
+  *out = reinterpret_cast<ulysses_t>(L);
+  return ULYSSES_OK;
+}
+
+void ulysses_destroy(ulysses_t h) {
+  Layer* L = reinterpret_cast<Layer*>(h);
+  if (!L) return;
+  cudaFree(L->d_status);
+  cudaFree(L->d_doc_offsets);
+  delete L;
+}
+
+int ulysses_workspace_size(ulysses_t h, size_t* bytes) {
+  const Layer* L = reinterpret_cast<const Layer*>(h);
+  if (!L || !bytes) return ULYSSES_ERR_INVALID_ARG;
+  const size_t per_rank_dq = (size_t)L->sl * L->bs * L->Hq * L->hs * sizeof(float);
+  const size_t per_rank_d = (size_t)L->bs * L->Hq * L->sl * sizeof(float);
+  *bytes = (size_t)L->P * (per_rank_dq + per_rank_d);
+  return ULYSSES_OK;
+}
+
+int ulysses_seq_to_head(ulysses_t h, int nheads, const void* const* seq_shards,
+                        void* const* head_shards, void* stream) {
+  const Layer* L = reinterpret_cast<const Layer*>(h);
+  if (!L) return ULYSSES_ERR_INVALID_ARG;
+  if (nheads != L->hc && nheads != L->hkv) return ULYSSES_ERR_INVALID_ARG;
+  if (L->empty()) return ULYSSES_OK;
+  CHECK_PTRS(seq_shards);
+  CHECK_PTRS(head_shards);
+  return uly::launch_seq_to_head(*L, nheads, seq_shards, head_shards, (cudaStream_t)stream);
+}
+
+int ulysses_head_to_seq(ulysses_t h, int nheads, const void* const* head_shards,
+                        void* const* seq_shards, void* stream) {
+  const Layer* L = reinterpret_cast<const Layer*>(h);
+  if (!L) return ULYSSES_ERR_INVALID_ARG;
+  if (nheads != L->hc && nheads != L->hkv) return ULYSSES_ERR_INVALID_ARG;
+  if (L->empty()) return ULYSSES_OK;
+  CHECK_PTRS(head_shards);
+  CHECK_PTRS(seq_shards);
+  return uly::launch_head_to_seq(*L, nheads, head_shards, seq_shards, (cudaStream_t)stream);
+}
+
+int ulysses_attn_fwd(ulysses_t h, const void* const* q, const void* const* k,
+                     const void* const* v, void* const* o, float* const* lse, void* stream) {
+  const Layer* L = reinterpret_cast<const Layer*>(h);
+  if (!L) return ULYSSES_ERR_INVALID_ARG;
+  if (L->empty()) return ULYSSES_OK;
+  CHECK_PTRS(q);
+  CHECK_PTRS(k);
+  CHECK_PTRS(v);
+  CHECK_PTRS(o);
+  CHECK_PTRS(lse);
+  return uly::launch_attn_fwd_simt(*L, q, k, v, o, lse, (cudaStream_t)stream);
+}
+
+int ulysses_attn_bwd(ulysses_t h, const void* const* q, const void* const* k,
+                     const void* const* v, const void* const* o, const void* const* dO,
+                     const float* const* lse, void* const* dq, void* const* dk, void* const* dv,
+                     void* workspace, void* stream) {
+  const Layer* L = reinterpret_cast<const Layer*>(h);
+  if (!L) return ULYSSES_ERR_INVALID_ARG;
+  if (L->empty()) return ULYSSES_OK;
+  CHECK_PTRS(q);
+  CHECK_PTRS(k);
+  CHECK_PTRS(v);
+  CHECK_PTRS(o);
+  CHECK_PTRS(dO);
+  CHECK_PTRS(lse);
+  CHECK_PTRS(dq);
+  CHECK_PTRS(dk);
+  CHECK_PTRS(dv);
+  if (!workspace) return ULYSSES_ERR_INVALID_ARG;
+  if (((uintptr_t)workspace) & 15u) return ULYSSES_ERR_ALIGNMENT;
+  return uly::launch_attn_bwd_simt(*L, q, k, v, o, dO, lse, dq, dk, dv, workspace,
+                                   (cudaStream_t)stream);
+}
+
+uint64_t ulysses_launch_count(void) { return uly::g_launches.load(std::memory_order_relaxed); }
+
+int ulysses_get_status(ulysses_t h) {
+  const Layer* L = reinterpret_cast<const Layer*>(h);
+  if (!L) return ULYSSES_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ULYSSES_ERR_CUDA;
+  unsigned word = 0;
+  if (cudaMemcpy(&word, L->d_status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ULYSSES_ERR_CUDA;
+  if (cudaMemset(L->d_status, 0, sizeof(unsigned)) != cudaSuccess) return ULYSSES_ERR_CUDA;
+  if (word & uly::STATUS_TIMEOUT) return ULYSSES_ERR_TIMEOUT;
+  return ULYSSES_OK;
+}
+
+}  // extern "C"

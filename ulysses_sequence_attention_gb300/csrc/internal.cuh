@@ -1,0 +1,116 @@
+// internal.cuh — shared host/device definitions of the Ulysses layer library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <vector>
+
+#include "../../include/ulysses.h"
+
+namespace uly {
+
+// Bits of the device status word (see ulysses_get_status).
+enum : unsigned {
+  STATUS_TIMEOUT = 1u,
+};
+
+struct Layer {
+  int64_t sl = 0, bs = 0;
+  int hc = 0, hkv = 0, hs = 0, P = 0, causal = 1, dtype = ULYSSES_BF16;
+  int Hq = 0;       // query heads per rank (hc / P)
+  int Hk = 0;       // kv heads per rank (hkv / P, or 1 when replicated)
+  int ndoc = 1;
+  std::vector<int32_t> doc_offsets;   // host copy, ndoc + 1 entries
+  int32_t* d_doc_offsets = nullptr;   // device copy, ndoc + 1 entries
+  unsigned* d_status = nullptr;       // device status word
+  int device = 0;
+  int64_t n() const { return sl / P; }          // tokens per sequence shard
+  int esize() const { return dtype == ULYSSES_BF16 ? 2 : 4; }
+  bool empty() const { return sl == 0 || bs == 0; }
+};
+
+// Per-rank pointer tables passed by value as kernel parameters.
+struct RankPtrs {
+  const void* p[ULYSSES_MAX_P];
+};
+struct RankPtrsMut {
+  void* p[ULYSSES_MAX_P];
+};
+
+// Shape of the per-rank attention problem, shared by the attention kernels.
+struct AttnShape {
+  int sl;          // global sequence length (<= 2^30)
+  int bs;
+  int P;
+  int Hq;          // query heads per rank
+  int Hk;          // kv heads per rank
+  int group;       // query heads per kv head on a rank (Hq / Hk)
+  int hs;
+  int causal;
+  int ndoc;
+  float scale;     // 1 / sqrt(hs)
+  float scale_log2;  // scale * log2(e)
+  const int32_t* doc_offsets;  // device, ndoc + 1
+  unsigned* status;
+};
+
+AttnShape make_shape(const Layer& L);
+
+// Host launchers (each returns a ulysses_status).
+int launch_seq_to_head(const Layer& L, int nheads, const void* const* src, void* const* dst,
+                       cudaStream_t s);
+int launch_head_to_seq(const Layer& L, int nheads, const void* const* src, void* const* dst,
+                       cudaStream_t s);
+int launch_attn_fwd_simt(const Layer& L, const void* const* q, const void* const* k,
+                         const void* const* v, void* const* o, float* const* lse, cudaStream_t s);
+int launch_attn_bwd_simt(const Layer& L, const void* const* q, const void* const* k,
+                         const void* const* v, const void* const* o, const void* const* dO,
+                         const float* const* lse, void* const* dq, void* const* dk,
+                         void* const* dv, void* workspace, cudaStream_t s);
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA; }
+
+// Adds n to the library-wide kernel launch counter (ulysses_launch_count).
+void count_launches(int n);
+
+}  // namespace uly
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+namespace uly {
+
+// Document index of position t: the largest d with doc_offsets[d] <= t.
+__device__ __forceinline__ int doc_of(const int32_t* offs, int ndoc, int t) {
+  int lo = 0, hi = ndoc - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (offs[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+}  // namespace uly

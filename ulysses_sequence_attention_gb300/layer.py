@@ -1,0 +1,86 @@
+"""UlyssesLayer: the layer's forward and backward on P virtual ranks of one GPU.
+
+The steps follow the HF blog "Ulysses Sequence Parallelism: Training with
+Million-Token Contexts" (algorithm steps 3 to 5) and their reverse for the
+backward:
+
+  forward:  Q, K, V seq->head  ->  attention forward  ->  O head->seq
+  backward: dO seq->head  ->  attention backward  ->  dQ, dK, dV head->seq
+
+Every step is one C-ABI call into libulysses.so. This class only owns the
+intermediate head-shard buffers (torch device memory) and enqueues the calls
+on the current stream.
+"""
+from __future__ import annotations
+
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import _binding as B
+
+
+class UlyssesLayer:
+    def __init__(self, sl: int, bs: int, hc: int, hkv: int, hs: int, P: int, causal: bool = True,
+                 doc_offsets: Optional[Sequence[int]] = None, dtype=torch.bfloat16,
+                 device: str = "cuda"):
+        self.h = B.ulysses_create(sl, bs, hc, hkv, hs, P, causal, doc_offsets, dtype)
+        self.sl, self.bs, self.hc, self.hkv, self.hs, self.P = sl, bs, hc, hkv, hs, P
+        self.dtype = dtype
+        self.device = device
+        self.Hq, self.Hk = self.h.Hq, self.h.Hk
+        self._bufs = None
+
+    # -- buffers -----------------------------------------------------------
+    def _alloc(self, backward: bool):
+        P, sl, bs, hs, dt, dev = self.P, self.sl, self.bs, self.hs, self.dtype, self.device
+        n = sl // P
+
+        def heads(H):
+            return [torch.empty((sl, bs, H, hs), dtype=dt, device=dev) for _ in range(P)]
+
+        b = self._bufs or {}
+        if "qh" not in b:
+            b["qh"], b["kh"], b["vh"], b["oh"] = heads(self.Hq), heads(self.Hk), heads(self.Hk), heads(self.Hq)
+            b["lse"] = [torch.empty((bs, self.Hq, sl), dtype=torch.float32, device=dev) for _ in range(P)]
+        if backward and "doh" not in b:
+            b["doh"], b["dqh"], b["dkh"], b["dvh"] = heads(self.Hq), heads(self.Hq), heads(self.Hk), heads(self.Hk)
+            nbytes = B.ulysses_workspace_size(self.h)
+            b["ws"] = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=dev)
+        self._bufs = b
+        return b
+
+    def new_seq_shards(self, H: int) -> List[torch.Tensor]:
+        n = self.sl // self.P
+        return [torch.empty((n, self.bs, H, self.hs), dtype=self.dtype, device=self.device)
+                for _ in range(self.P)]
+
+    # -- steps -------------------------------------------------------------
+    def forward(self, q_seq, k_seq, v_seq, o_seq, stream=None):
+        """Seq-sharded Q, K, V in, seq-sharded O out (all lists of P tensors)."""
+        b = self._alloc(backward=False)
+        B.ulysses_seq_to_head(self.h, self.hc, q_seq, b["qh"], stream)
+        B.ulysses_seq_to_head(self.h, self.hkv, k_seq, b["kh"], stream)
+        B.ulysses_seq_to_head(self.h, self.hkv, v_seq, b["vh"], stream)
+        B.ulysses_attn_fwd(self.h, b["qh"], b["kh"], b["vh"], b["oh"], b["lse"], stream)
+        B.ulysses_head_to_seq(self.h, self.hc, b["oh"], o_seq, stream)
+        return o_seq
+
+    def backward(self, do_seq, dq_seq, dk_seq, dv_seq, stream=None):
+        """Seq-sharded dO in, seq-sharded dQ, dK, dV out. Uses the last forward's state."""
+        b = self._alloc(backward=True)
+        B.ulysses_seq_to_head(self.h, self.hc, do_seq, b["doh"], stream)
+        B.ulysses_attn_bwd(self.h, b["qh"], b["kh"], b["vh"], b["oh"], b["doh"], b["lse"],
+                           b["dqh"], b["dkh"], b["dvh"], b["ws"], stream)
+        B.ulysses_head_to_seq(self.h, self.hc, b["dqh"], dq_seq, stream)
+        B.ulysses_head_to_seq(self.h, self.hkv, b["dkh"], dk_seq, stream)
+        B.ulysses_head_to_seq(self.h, self.hkv, b["dvh"], dv_seq, stream)
+        return dq_seq, dk_seq, dv_seq
+
+    @property
+    def lse(self):
+        return self._bufs["lse"]
+
+    @property
+    def head_buffers(self):
+        return self._bufs
