@@ -85,6 +85,9 @@ PARITY = [
     (256, 1, 4, 4, 64, 1, torch.bfloat16, True, None, 7),          # P = 1, hs 64
     (96, 1, 2, 1, 32, 2, torch.float32, True, [0, 1, 2, 96], 8),   # single-token documents
     (2, 1, 2, 2, 128, 2, torch.bfloat16, True, None, 9),           # two tokens in all
+    (2048, 1, 32, 8, 128, 8, torch.bfloat16, True, None, 11),      # Llama-8B heads, GQA group 4
+    (2048, 1, 32, 8, 128, 8, torch.bfloat16, True, [0, 57, 700, 1500, 2048], 12),  # packed
+    (1152, 1, 6, 2, 128, 2, torch.bfloat16, True, None, 13),       # group 3: a pair and a single
 ]
 
 

@@ -127,9 +127,22 @@ int ulysses_create(ulysses_t* out, int64_t sl, int64_t bs, int hc, int hkv, int 
   if (e == cudaSuccess)
     e = cudaMemcpy(L->d_doc_offsets, L->doc_offsets.data(), sizeof(int32_t) * (L->ndoc + 1),
                    cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && uly::fwd_sm103_supported(*L) && !L->empty()) {
+    std::vector<int2> kv_range;
+    std::vector<int> order;
+    uly::plan_tiles(*L, kv_range, order);
+    e = cudaMalloc(&L->d_kv_range, sizeof(int2) * kv_range.size());
+    if (e == cudaSuccess) e = cudaMalloc(&L->d_m_order, sizeof(int) * order.size());
+    if (e == cudaSuccess)
+      e = cudaMemcpy(L->d_kv_range, kv_range.data(), sizeof(int2) * kv_range.size(), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(L->d_m_order, order.data(), sizeof(int) * order.size(), cudaMemcpyHostToDevice);
+  }
   if (e != cudaSuccess) {
     cudaFree(L->d_status);
     cudaFree(L->d_doc_offsets);
+    cudaFree(L->d_kv_range);
+    cudaFree(L->d_m_order);
     delete L;
     return ULYSSES_ERR_CUDA;
   }
@@ -142,6 +155,8 @@ void ulysses_destroy(ulysses_t h) {
   if (!L) return;
   cudaFree(L->d_status);
   cudaFree(L->d_doc_offsets);
+  cudaFree(L->d_kv_range);
+  cudaFree(L->d_m_order);
   delete L;
 }
 
@@ -186,6 +201,8 @@ int ulysses_attn_fwd(ulysses_t h, const void* const* q, const void* const* k,
   CHECK_PTRS(v);
   CHECK_PTRS(o);
   CHECK_PTRS(lse);
+  if (uly::fwd_sm103_supported(*L))
+    return uly::launch_attn_fwd_sm103(*L, q, k, v, o, lse, (cudaStream_t)stream);
   return uly::launch_attn_fwd_simt(*L, q, k, v, o, lse, (cudaStream_t)stream);
 }
 

@@ -25,6 +25,11 @@ struct Layer {
   int32_t* d_doc_offsets = nullptr;   // device copy, ndoc + 1 entries
   unsigned* d_status = nullptr;       // device status word
   int device = 0;
+  // Tensor-core path: key-tile range per 128-row query tile, and the query
+  // tiles ordered by their number of key tiles (most first). Device copies.
+  int2* d_kv_range = nullptr;
+  int* d_m_order = nullptr;
+  long long timeout_cycles = 4000000000LL;  // bound of every device-side wait (~2 s)
   int64_t n() const { return sl / P; }          // tokens per sequence shard
   int esize() const { return dtype == ULYSSES_BF16 ? 2 : 4; }
   bool empty() const { return sl == 0 || bs == 0; }
@@ -68,6 +73,11 @@ int launch_attn_bwd_simt(const Layer& L, const void* const* q, const void* const
                          const void* const* v, const void* const* o, const void* const* dO,
                          const float* const* lse, void* const* dq, void* const* dk,
                          void* const* dv, void* workspace, cudaStream_t s);
+
+bool fwd_sm103_supported(const Layer& L);
+void plan_tiles(const Layer& L, std::vector<int2>& kv_range, std::vector<int>& order);
+int launch_attn_fwd_sm103(const Layer& L, const void* const* q, const void* const* k, const void* const* v,
+                          void* const* o, float* const* lse, cudaStream_t s);
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA; }
 
