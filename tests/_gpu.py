@@ -31,7 +31,13 @@ def errors(gpu: torch.Tensor, ref: torch.Tensor):
     return float(d.max()), float(d.mean())
 
 
-def assert_close(name, gpu, ref, dtype):
+def assert_close(name, gpu, ref, dtype, check_mean=True):
+    """Element-wise bound; the mean-abs bound too unless the sample is biased.
+
+    A sample chosen for its large values (keys at document starts, say) is not
+    a fair sample for a whole-tensor mean: for those, only the element-wise
+    bound applies.
+    """
     t = TOL[dtype]
     g = gpu.detach().cpu().to(F64)
     r = ref.cpu().to(F64)
@@ -44,7 +50,8 @@ def assert_close(name, gpu, ref, dtype):
     worst = float((d / bound).max())
     assert worst <= 1.0, (f"{name}: |x-ref| exceeds atol {t['atol']} + rtol {t['rtol']:.3g}*|ref| "
                           f"(worst ratio {worst:.3g}, max-abs {mx:.3g})")
-    assert mean <= t["mean"], f"{name}: mean-abs {mean:.3g} > {t['mean']}"
+    if check_mean:
+        assert mean <= t["mean"], f"{name}: mean-abs {mean:.3g} > {t['mean']}"
     return mx, mean
 
 

@@ -83,8 +83,11 @@ def check_rows(w, x, got, heads, rows_per_head, seed):
         assert_close("dQ rows", torch.cat(errs["dq"]), torch.cat(refs["dq"]), w.torch_dtype)
 
 
-def check_cols(w, x, got, kv_heads, cols, row_chunk=2048):
-    """dK and dV at sampled key rows of some kv heads (sums over the GQA group)."""
+def check_cols(w, x, got, kv_heads, cols, row_chunk=2048, uniform=True):
+    """dK and dV at sampled key rows of some kv heads (sums over the GQA group).
+
+    ``uniform``: the keys are a uniform sample, so the mean-abs bound applies.
+    """
     offs = doc_offsets_for(w)
     s = 1.0 / math.sqrt(w.hs)
     g = w.hc // w.hkv
@@ -103,8 +106,8 @@ def check_cols(w, x, got, kv_heads, cols, row_chunk=2048):
         gv.append(got["dv"][cols, 0, kv])
         rk.append(dk)
         rv.append(dv)
-    assert_close("dK cols", torch.cat(gk), torch.cat(rk), w.torch_dtype)
-    assert_close("dV cols", torch.cat(gv), torch.cat(rv), w.torch_dtype)
+    assert_close("dK cols", torch.cat(gk), torch.cat(rk), w.torch_dtype, check_mean=uniform)
+    assert_close("dV cols", torch.cat(gv), torch.cat(rv), w.torch_dtype, check_mean=uniform)
 
 
 def test_llama8b_8k_forward(u):
@@ -135,10 +138,12 @@ def test_packed_64k_forward_backward(u):
     check_rows(w, x, got, heads=range(0, w.hc, 3), rows_per_head=24, seed=84)
     offs = doc_offsets_for(w)
     rng = np.random.default_rng(85)
-    # keys next to document boundaries and at random places
-    near = [o + d for o in offs[1:-1] for d in (-1, 0, 1)]
-    cols = torch.tensor(sorted(set(near[:18] + list(rng.choice(w.sl, 6, replace=False)))))
-    check_cols(w, x, got, kv_heads=[2], cols=cols, row_chunk=4096)
+    # keys next to document boundaries (first keys of documents carry the
+    # largest gradients: element-wise bound only), then keys at random places
+    near = sorted({o + d for o in offs[1:-1] for d in (-1, 0, 1)})
+    check_cols(w, x, got, kv_heads=[2], cols=torch.tensor(near[:18]), row_chunk=4096, uniform=False)
+    check_cols(w, x, got, kv_heads=[6], cols=torch.tensor(np.sort(rng.choice(w.sl, 12, replace=False))),
+               row_chunk=4096)
 
 
 @pytest.mark.slow

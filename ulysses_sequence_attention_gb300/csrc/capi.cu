@@ -137,12 +137,23 @@ int ulysses_create(ulysses_t* out, int64_t sl, int64_t bs, int hc, int hkv, int 
       e = cudaMemcpy(L->d_kv_range, kv_range.data(), sizeof(int2) * kv_range.size(), cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
       e = cudaMemcpy(L->d_m_order, order.data(), sizeof(int) * order.size(), cudaMemcpyHostToDevice);
+    std::vector<int2> q_range;
+    std::vector<int> n_order;
+    uly::plan_bwd_tiles(*L, q_range, n_order);
+    if (e == cudaSuccess) e = cudaMalloc(&L->d_q_range, sizeof(int2) * q_range.size());
+    if (e == cudaSuccess) e = cudaMalloc(&L->d_n_order, sizeof(int) * n_order.size());
+    if (e == cudaSuccess)
+      e = cudaMemcpy(L->d_q_range, q_range.data(), sizeof(int2) * q_range.size(), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(L->d_n_order, n_order.data(), sizeof(int) * n_order.size(), cudaMemcpyHostToDevice);
   }
   if (e != cudaSuccess) {
     cudaFree(L->d_status);
     cudaFree(L->d_doc_offsets);
     cudaFree(L->d_kv_range);
     cudaFree(L->d_m_order);
+    cudaFree(L->d_q_range);
+    cudaFree(L->d_n_order);
     delete L;
     return ULYSSES_ERR_CUDA;
   }
@@ -157,6 +168,8 @@ void ulysses_destroy(ulysses_t h) {
   cudaFree(L->d_doc_offsets);
   cudaFree(L->d_kv_range);
   cudaFree(L->d_m_order);
+  cudaFree(L->d_q_range);
+  cudaFree(L->d_n_order);
   delete L;
 }
 
@@ -224,6 +237,8 @@ int ulysses_attn_bwd(ulysses_t h, const void* const* q, const void* const* k,
   CHECK_PTRS(dv);
   if (!workspace) return ULYSSES_ERR_INVALID_ARG;
   if (((uintptr_t)workspace) & 15u) return ULYSSES_ERR_ALIGNMENT;
+  if (uly::fwd_sm103_supported(*L))
+    return uly::launch_attn_bwd_sm103(*L, q, k, v, o, dO, lse, dq, dk, dv, workspace, (cudaStream_t)stream);
   return uly::launch_attn_bwd_simt(*L, q, k, v, o, dO, lse, dq, dk, dv, workspace,
                                    (cudaStream_t)stream);
 }

@@ -29,6 +29,9 @@ struct Layer {
   // tiles ordered by their number of key tiles (most first). Device copies.
   int2* d_kv_range = nullptr;
   int* d_m_order = nullptr;
+  // Backward: query-tile range per 128-row key tile, key tiles ordered by work.
+  int2* d_q_range = nullptr;
+  int* d_n_order = nullptr;
   long long timeout_cycles = 4000000000LL;  // bound of every device-side wait (~2 s)
   int64_t n() const { return sl / P; }          // tokens per sequence shard
   int esize() const { return dtype == ULYSSES_BF16 ? 2 : 4; }
@@ -78,6 +81,11 @@ bool fwd_sm103_supported(const Layer& L);
 void plan_tiles(const Layer& L, std::vector<int2>& kv_range, std::vector<int>& order);
 int launch_attn_fwd_sm103(const Layer& L, const void* const* q, const void* const* k, const void* const* v,
                           void* const* o, float* const* lse, cudaStream_t s);
+
+void plan_bwd_tiles(const Layer& L, std::vector<int2>& q_range, std::vector<int>& order);
+int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* const* k, const void* const* v,
+                          const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,
+                          void* const* dk, void* const* dv, void* workspace, cudaStream_t s);
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA; }
 
