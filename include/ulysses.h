@@ -63,7 +63,8 @@ typedef enum ulysses_status {
   ULYSSES_ERR_ALIGNMENT = -3,    /* a device pointer is not 16-byte aligned */
   ULYSSES_ERR_UNSUPPORTED = -4,  /* valid for the method, but outside what this build implements */
   ULYSSES_ERR_CUDA = -5,         /* a CUDA runtime call failed (allocation, launch) */
-  ULYSSES_ERR_TIMEOUT = -6       /* a device-side bounded wait ran out (reported by ulysses_get_status) */
+  ULYSSES_ERR_TIMEOUT = -6,      /* a device-side bounded wait ran out (reported by ulysses_get_status) */
+  ULYSSES_ERR_TOO_LARGE = -7     /* ulysses_attn_bwd_noalloc: the call needs more scratch than the library holds */
 } ulysses_status;
 
 typedef enum ulysses_dtype {
@@ -207,6 +208,47 @@ int ulysses_get_status(ulysses_t h);
  * region made. Never fails.
  */
 uint64_t ulysses_launch_count(void);
+
+/*
+ * ulysses_attn_bwd_noalloc — ulysses_attn_bwd for callers that cannot allocate
+ * device memory. There is no counterpart in the paper: this is a deployment
+ * convenience of this library.
+ *
+ * Who needs it: code that runs inside another runtime which owns the GPU's
+ * memory. Examples are a plugin that is handed only its input and output
+ * buffers, a server that reserves all device memory at start-up and must not
+ * allocate while it serves, and a framework whose caching allocator has to
+ * account for every byte. Such callers cannot call cudaMalloc for the
+ * workspace that ulysses_attn_bwd takes. cudaMalloc can also synchronise the
+ * device, which stalls work on other streams.
+ *
+ * Arguments and results are those of ulysses_attn_bwd, without `workspace`.
+ * The workspace is a file-scope device array of
+ * ULYSSES_NOALLOC_SCRATCH_BYTES bytes inside the library. Every GPU that loads
+ * the library holds this array until the process exits. This call never
+ * calls cudaMalloc, cudaFree or any allocating library routine. The handle
+ * still comes from ulysses_create, which allocates a few bytes of metadata:
+ * create it during set-up.
+ *
+ * Limits and sharing:
+ *  - A layer whose backward needs more than ULYSSES_NOALLOC_SCRATCH_BYTES of
+ *    workspace (see ulysses_workspace_size) is rejected with
+ *    ULYSSES_ERR_TOO_LARGE before anything is enqueued. For the Llama-8B head
+ *    shape (32 query heads, head size 128, bf16) that allows about 4K tokens.
+ *  - Every call shares the one array, and it keeps the last call's contents.
+ *    Each call clears the parts that must start at zero itself. Two calls that
+ *    overlap on the GPU (on different streams, or different host threads
+ *    without ordering) race on the array and corrupt each other's dQ: order
+ *    them.
+ *  - The first call on a device looks up the array's device address with
+ *    cudaGetSymbolAddress (once per device, with that device current). Make
+ *    that first call before any stream capture begins.
+ */
+#define ULYSSES_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+int ulysses_attn_bwd_noalloc(ulysses_t h, const void* const* q, const void* const* k,
+                             const void* const* v, const void* const* o, const void* const* dO,
+                             const float* const* lse, void* const* dq, void* const* dk,
+                             void* const* dv, void* stream);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,89 @@
+"""The backward entry point that allocates nothing: ulysses_attn_bwd_noalloc.
+
+Some callers of this library cannot allocate device memory. Examples are a
+plugin that a host runtime hands only its input and output buffers, a server
+that reserves all GPU memory at start-up and must not allocate while it
+serves, and a framework whose caching allocator must see every byte. They
+cannot provide the workspace that ulysses_attn_bwd takes.
+ulysses_attn_bwd_noalloc runs the same backward on a fixed scratch array inside
+the library. These tests call it through the C ABI and check it against the
+allocating entry point: two calls in a row, because the array keeps the last
+call's contents and each call must clear what has to start at zero.
+
+This file is named so that pytest collects it last. A run that stops at the
+first failure has then already run every other test.
+"""
+import pytest
+import torch
+
+from tests._gpu import assert_close
+from workloads import random_inputs, split_shards
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def u():
+    import ulysses_sequence_attention_gb300 as pkg
+    return pkg
+
+
+def _forward(u, sl, hc, hkv, P, seed, offs=None):
+    x = random_inputs(sl, 1, hc, hkv, 128, torch.bfloat16, seed)
+    L = u.UlyssesLayer(sl, 1, hc, hkv, 128, P, True, offs, torch.bfloat16)
+    cu = lambda t: [s.cuda() for s in split_shards(t, P)]  # noqa: E731
+    o = L.new_seq_shards(hc)
+    L.forward(cu(x["q"]), cu(x["k"]), cu(x["v"]), o)
+    L._alloc(backward=True)
+    b = L.head_buffers
+    u.ulysses_seq_to_head(L.h, hc, cu(x["do"]), b["doh"])
+    return L, b
+
+
+def _grads(L, hk_shape):
+    P = L.P
+    dq = [torch.full_like(t, float("nan")) for t in L.head_buffers["qh"]]
+    dk = [torch.full_like(t, float("nan")) for t in L.head_buffers["kh"]]
+    dv = [torch.full_like(t, float("nan")) for t in L.head_buffers["vh"]]
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("sl,hc,hkv,P,offs", [
+    (1024, 32, 8, 8, None),                    # Llama-8B heads
+    (1000, 8, 2, 4, [0, 333, 334, 1000]),      # ragged tail, packed documents, replicated kv
+])
+def test_noalloc_matches_the_allocating_entry_point(u, sl, hc, hkv, P, offs):
+    L, b = _forward(u, sl, hc, hkv, P, seed=31, offs=offs)
+    assert u.ulysses_workspace_size(L.h) <= u.ULYSSES_NOALLOC_SCRATCH_BYTES
+    args = (b["qh"], b["kh"], b["vh"], b["oh"], b["doh"], b["lse"])
+    ref = _grads(L, None)
+    u.ulysses_attn_bwd(L.h, *args, *ref, b["ws"])
+    torch.cuda.synchronize()
+    assert u.ulysses_get_status(L.h) == u.ULYSSES_OK
+    for call in range(2):
+        got = _grads(L, None)
+        u.ulysses_attn_bwd_noalloc(L.h, *args, *got)
+        torch.cuda.synchronize()
+        assert u.ulysses_get_status(L.h) == u.ULYSSES_OK
+        for name, gs, rs in zip(("dq", "dk", "dv"), got, ref):
+            for r in range(P):
+                assert_close(f"{name}[{r}] call {call}", gs[r], rs[r], torch.bfloat16)
+        # dK and dV take no atomics: the two entry points agree bit for bit
+        for gs, rs in zip(got[1:], ref[1:]):
+            for r in range(P):
+                assert torch.equal(gs[r], rs[r])
+
+
+def test_noalloc_rejects_a_layer_beyond_its_scratch(u):
+    # 65536 tokens x 2 query heads x (128 + 1) fp32 = 64.5 MiB of workspace > 64 MiB
+    sl, hc, P = 65536, 2, 1
+    h = u.ulysses_create(sl, 1, hc, hc, 128, P, True, None, torch.bfloat16)
+    assert u.ulysses_workspace_size(h) > u.ULYSSES_NOALLOC_SCRATCH_BYTES
+    t = [torch.zeros((sl, 1, hc, 128), dtype=torch.bfloat16, device="cuda")]
+    lse = [torch.zeros((1, hc, sl), dtype=torch.float32, device="cuda")]
+    n0 = u.ulysses_launch_count()
+    with pytest.raises(u.UlyssesError) as ei:
+        u.ulysses_attn_bwd_noalloc(h, t, t, t, t, t, lse, t, t, t)
+    assert ei.value.status == u.ULYSSES_ERR_TOO_LARGE
+    assert u.ulysses_launch_count() == n0   # rejected before anything was enqueued
+    h.destroy()

@@ -7,8 +7,9 @@ CUDA library has not been built: there is no fallback path.
 """
 from ._binding import (  # noqa: F401
     LIB_PATH, ULYSSES_BF16, ULYSSES_ERR_ALIGNMENT, ULYSSES_ERR_CUDA, ULYSSES_ERR_DIVISIBILITY,
-    ULYSSES_ERR_INVALID_ARG, ULYSSES_ERR_TIMEOUT, ULYSSES_ERR_UNSUPPORTED, ULYSSES_FP32,
-    ULYSSES_MAX_P, ULYSSES_OK, UlyssesError, UlyssesHandle, ulysses_attn_bwd, ulysses_attn_fwd,
+    ULYSSES_ERR_INVALID_ARG, ULYSSES_ERR_TIMEOUT, ULYSSES_ERR_TOO_LARGE, ULYSSES_ERR_UNSUPPORTED, ULYSSES_FP32,
+    ULYSSES_MAX_P, ULYSSES_OK, ULYSSES_NOALLOC_SCRATCH_BYTES, UlyssesError, UlyssesHandle, ulysses_attn_bwd,
+    ulysses_attn_bwd_noalloc, ulysses_attn_fwd,
     ulysses_create, ulysses_destroy, ulysses_get_status, ulysses_head_to_seq, ulysses_launch_count, ulysses_seq_to_head,
     ulysses_strerror, ulysses_workspace_size,
 )

@@ -25,6 +25,8 @@ ULYSSES_ERR_ALIGNMENT = -3
 ULYSSES_ERR_UNSUPPORTED = -4
 ULYSSES_ERR_CUDA = -5
 ULYSSES_ERR_TIMEOUT = -6
+ULYSSES_ERR_TOO_LARGE = -7
+ULYSSES_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 ULYSSES_BF16 = 0
 ULYSSES_FP32 = 1
 ULYSSES_MAX_P = 128
@@ -61,6 +63,8 @@ lib.ulysses_attn_bwd.argtypes = [_vp] + [_pp] * 9 + [_vp, _vp]
 lib.ulysses_attn_bwd.restype = ctypes.c_int
 lib.ulysses_get_status.argtypes = [_vp]
 lib.ulysses_get_status.restype = ctypes.c_int
+lib.ulysses_attn_bwd_noalloc.argtypes = [_vp] + [_pp] * 9 + [_vp]
+lib.ulysses_attn_bwd_noalloc.restype = ctypes.c_int
 lib.ulysses_launch_count.argtypes = []
 lib.ulysses_launch_count.restype = ctypes.c_uint64
 
@@ -219,3 +223,19 @@ def ulysses_get_status(h: UlyssesHandle) -> int:
 
 def ulysses_launch_count() -> int:
     return int(lib.ulysses_launch_count())
+
+
+def ulysses_attn_bwd_noalloc(h: UlyssesHandle, q, k, v, o, do, lse, dq, dk, dv, stream=None):
+    """ulysses_attn_bwd on the library's built-in scratch: no workspace argument.
+
+    For callers that may not allocate device memory. See the C header for the
+    size limit and for the sharing rules of the built-in scratch.
+    """
+    dt = h.torch_dtype
+    nq = h.sl * h.bs * h.Hq * h.hs
+    nk = h.sl * h.bs * h.Hk * h.hs
+    args = [_ptrs(h, q, nq, dt, "q"), _ptrs(h, k, nk, dt, "k"), _ptrs(h, v, nk, dt, "v"),
+            _ptrs(h, o, nq, dt, "o"), _ptrs(h, do, nq, dt, "do"),
+            _ptrs(h, lse, h.bs * h.Hq * h.sl, torch.float32, "lse"),
+            _ptrs(h, dq, nq, dt, "dq"), _ptrs(h, dk, nk, dt, "dk"), _ptrs(h, dv, nk, dt, "dv")]
+    _check(lib.ulysses_attn_bwd_noalloc(h.ptr, *args, _stream(stream)), "ulysses_attn_bwd_noalloc")

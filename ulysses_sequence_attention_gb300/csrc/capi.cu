@@ -67,6 +67,7 @@ const char* ulysses_strerror(int status) {
     case ULYSSES_ERR_UNSUPPORTED: return "unsupported configuration";
     case ULYSSES_ERR_CUDA: return "CUDA runtime error";
     case ULYSSES_ERR_TIMEOUT: return "device-side wait timed out";
+    case ULYSSES_ERR_TOO_LARGE: return "the backward needs more scratch than the library's built-in array";
     default: return "unknown status";
   }
 }

@@ -1,0 +1,55 @@
+// noalloc.cu — the backward pass for callers that cannot allocate device memory.
+//
+// ulysses_attn_bwd takes its workspace from the caller. Callers inside a host
+// runtime that owns the GPU's memory (a plugin given only its buffers, a
+// server that must not allocate after start-up, a framework allocator that
+// tracks every byte) have no way to provide one. This file holds a fixed
+// workspace in the library itself and runs the unchanged backward on it.
+#include <mutex>
+
+#include "internal.cuh"
+
+namespace {
+
+// The workspace of ulysses_attn_bwd_noalloc: the fp32 dQ accumulators and the
+// D rows. It lives for the lifetime of the process on every device that loads
+// the library. Calls share it; the backward zeroes the accumulators itself.
+static __device__ __align__(256) unsigned char g_bwd_scratch[ULYSSES_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_bwd_scratch for each device. In host code the symbol is
+// only a host-side stand-in, so the address comes from cudaGetSymbolAddress,
+// once per device, with that device current.
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+int scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ULYSSES_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return ULYSSES_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p) return ULYSSES_ERR_CUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return ULYSSES_OK;
+}
+
+}  // namespace
+
+extern "C" int ulysses_attn_bwd_noalloc(ulysses_t h, const void* const* q, const void* const* k,
+                                        const void* const* v, const void* const* o, const void* const* dO,
+                                        const float* const* lse, void* const* dq, void* const* dk,
+                                        void* const* dv, void* stream) {
+  if (!h) return ULYSSES_ERR_INVALID_ARG;
+  size_t need = 0;
+  int st = ulysses_workspace_size(h, &need);
+  if (st != ULYSSES_OK) return st;
+  if (need > (size_t)ULYSSES_NOALLOC_SCRATCH_BYTES) return ULYSSES_ERR_TOO_LARGE;
+  void* scratch = nullptr;
+  st = scratch_address(&scratch);
+  if (st != ULYSSES_OK) return st;
+  return ulysses_attn_bwd(h, q, k, v, o, dO, lse, dq, dk, dv, scratch, stream);
+}
