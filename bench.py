@@ -168,6 +168,8 @@ def run_ours(args, w, rank, world):
         if timed:
             mark("fwd1")
         B.ulysses_head_to_seq(h, w.hc, b["oh"], o)
+        if timed:
+            mark("h2s1")
         if w.backward:
             B.ulysses_seq_to_head(h, w.hc, seq["do"], b["doh"])
             if timed:
@@ -217,6 +219,7 @@ def run_ours(args, w, rank, world):
 
     fwd_ms = statistics.mean(span("fwd0", "fwd1"))
     s2h_ms = statistics.mean(span("s2h0", "fwd0"))
+    h2s_ms = statistics.mean(span("fwd1", "h2s1"))
     bwd_ms = statistics.mean(span("bwd0", "bwd1")) if w.backward else 0.0
 
     # max over ranks
@@ -233,7 +236,7 @@ def run_ours(args, w, rank, world):
         e2e = run_e2e(args, w, L, x, dev, world, barrier)
 
     result = {"ms_per_step": ms_per_step, "value": value, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
-              "s2h_qkv_ms": s2h_ms, "launches": launches, "clocks": clk, "e2e": e2e}
+              "s2h_qkv_ms": s2h_ms, "h2s_o_ms": h2s_ms, "launches": launches, "clocks": clk, "e2e": e2e}
     return result
 
 
@@ -353,14 +356,16 @@ def workload_config(w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_32k", choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sl", type=int, default=4096, help="oracle sample length for cpu_baseline")
-    ap.add_argument("--ref-sl", type=int, default=2048, help="oracle sample length per reference step")
+    ap.add_argument("--ref-sl", type=int, default=1024, help="oracle sample length per reference step")
+    ap.add_argument("--sl", type=int, default=None,
+                    help="run the workload's shape at another sequence length (profiling a smaller case)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
@@ -368,6 +373,13 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     w = WORKLOADS[args.workload]
+    if args.sl is not None:
+        import dataclasses
+        if w.ndoc:
+            ap.error("--sl applies to single-document workloads")
+        if args.sl % w.P:
+            ap.error("--sl must be divisible by P")
+        w = dataclasses.replace(w, sl=args.sl, name=f"{w.name}@sl{args.sl}")
 
     if args.impl == "reference":
         run_reference(args, w, rank, world)
@@ -387,6 +399,7 @@ def main():
         bwd_tf = fl_bwd / (r["bwd_ms"] * 1e-3) / 1e12 if w.backward else None
         x_bytes = exchange_bytes(w, w.hc) + 2 * exchange_bytes(w, w.hkv)
         s2h_gbs = x_bytes / (r["s2h_qkv_ms"] * 1e-3) / 1e9
+        h2s_gbs = exchange_bytes(w, w.hc) / (r["h2s_o_ms"] * 1e-3) / 1e9
         sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
         if w.backward:
             dom = {"kernel": "ulysses_attn_bwd", "achieved": bwd_tf, "ms": r["bwd_ms"], "flops": fl_bwd}
@@ -419,8 +432,11 @@ def main():
                               "bwd_frac_sustained": (bwd_tf / sustained) if bwd_tf else None,
                               "fwd_tflop": fl_fwd / 1e12, "bwd_tflop": fl_bwd / 1e12},
                 "exchange": {"s2h_qkv_ms": r["s2h_qkv_ms"], "s2h_qkv_gbs": s2h_gbs,
-                             "s2h_qkv_frac_hbm": s2h_gbs / peaks["hbm_gbs"], "hbm_peak_gbs": peaks["hbm_gbs"],
-                             "hbm_peak_source": src},
+                             "s2h_qkv_frac_hbm": s2h_gbs / peaks["hbm_gbs"],
+                             "h2s_o_ms": r["h2s_o_ms"], "h2s_o_gbs": h2s_gbs,
+                             "h2s_o_frac_hbm": h2s_gbs / peaks["hbm_gbs"],
+                             "bytes_rule": "read + write of the whole tensor per exchange",
+                             "hbm_peak_gbs": peaks["hbm_gbs"], "hbm_peak_source": src},
                 "context": "pages' figure (not a target): ALST trains a 500K-token sequence for Llama-8B on one H100"}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -18,18 +18,21 @@
 //        dV += P^T dO,  dK += dS^T Q                      (accumulated in tensor memory)
 //        dQ_tile = dS K                                   (into tensor memory)
 //     and eight compute warps turn S^T, dP^T into P^T and dS^T (bf16) between
-//     the two halves. dQ_tile is added into the fp32 accumulator with vector
-//     reductions. At the end dK (scaled by s) and dV leave by TMA store.
+//     the two halves. A fourth warpgroup reads each dQ tile out of tensor
+//     memory, stages it in the consumed Q/dO stage and adds it into the fp32
+//     accumulator with TMA reduce-add (whole 128-byte lines at L2). At the end
+//     dK (scaled by s) and dV leave by TMA store.
 //  3. bwd_dq_convert: dQ = bf16(accumulator).
 //
 // Tensor memory: [0,128) S^T, then P^T (bf16) in [0,64); [128,256) dP^T, then
 // dS^T (bf16) in [128,192), then the dQ tile; [256,384) dV; [384,512) dK.
 // Reuse relies on UMMAs from one thread running in issue order.
 //
-// Warp roles (384 threads): warps 0-7 compute (thread = kv row / TMEM lane,
+// Warp roles (512 threads): warps 0-7 compute (thread = kv row / TMEM lane,
 // warp w handles columns [64*(w/4), 64*(w/4)+64)); warp 8 TMA and the LSE/D
 // rows; warp 9 UMMA and tensor-memory allocation; warps 10-11 complete the
-// third warpgroup. Every mbarrier wait is bounded.
+// third warpgroup; warps 12-15 move the dQ tiles. Every mbarrier wait is
+// bounded.
 #include <math.h>
 
 #include <algorithm>
@@ -45,9 +48,13 @@ namespace {
 using namespace sm103;
 
 constexpr int kRanksPerLaunch = 8;
-constexpr int kThreads = 384;
-constexpr int kRegsCompute = 224;
-constexpr int kRegsOther = 56;
+constexpr int kThreads = 512;
+// Registers: the block launches at 128 per thread; the compute warpgroups take
+// 192, the TMA/UMMA warpgroup keeps 56, the dQ warpgroup 72:
+// 2*128*192 + 128*56 + 128*72 = 512*128.
+constexpr int kRegsCompute = 192;
+constexpr int kRegsIssue = 56;
+constexpr int kRegsDq = 72;
 constexpr int NQ = 2;                              // Q/dO pipeline stages
 constexpr uint32_t kTile = 128 * 128 * 2;          // 32 KB
 constexpr uint32_t kOffK = 0;
@@ -66,9 +73,9 @@ struct BwdParams {
   CUtensorMap tdo[kRanksPerLaunch];
   CUtensorMap tdk[kRanksPerLaunch];
   CUtensorMap tdv[kRanksPerLaunch];
+  CUtensorMap tdq[kRanksPerLaunch];    // fp32 accumulator [sl][bs][Hq][128], boxes of 32 x 128
   const float* lse[kRanksPerLaunch];
   const float* D[kRanksPerLaunch];     // [bs][Hq][sl]
-  float* dq_acc[kRanksPerLaunch];      // [sl][bs][Hq][128]
   const int2* q_range;                 // per key tile: first and last query tile
   const int* n_order;                  // key tiles, most work first
   const int32_t* doc_offsets;
@@ -80,23 +87,20 @@ struct BwdParams {
 
 enum {
   B_KVFULL = 0,
-  B_QFULL = 1,                 // NQ
-  B_QEMPTY = B_QFULL + NQ,     // NQ
-  B_SFULL = B_QEMPTY + NQ,     // S^T and dP^T done
-  B_LOADED = B_SFULL + 1,      // compute warps hold S^T, dP^T in registers (256)
+  B_QFULL = 1,                 // NQ: Q, dO tiles and their LSE/D rows (32 arrivals + tx)
+  B_QEMPTY = B_QFULL + NQ,     // NQ: the stage's dQ reduction has read it (1)
+  B_SFULL = B_QEMPTY + NQ,     // S^T done (commit)
+  B_DPFULL = B_SFULL + 1,      // dP^T done (commit)
+  B_LOADED = B_DPFULL + 1,     // compute warps hold S^T, dP^T in registers (256)
   B_PFULL = B_LOADED + 1,      // P^T, dS^T written (256)
-  B_DQFULL = B_PFULL + 1,      // dQ tile done
-  B_DQEMPTY = B_DQFULL + 1,    // dQ tile read out (256)
-  B_DKDV = B_DQEMPTY + 1,      // every UMMA done
+  B_DQFULL = B_PFULL + 1,      // dQ tile done (commit)
+  B_DQEMPTY = B_DQFULL + 1,    // dQ tile read out of tensor memory (128)
+  B_STAGED = B_DQEMPTY + 1,    // dQ tile staged in shared memory (128)
+  B_DKDV = B_STAGED + 1,       // every UMMA done (commit)
   B_EPI = B_DKDV + 1,          // dK/dV staged (256)
   B_DRAIN = B_EPI + 1,
   B_COUNT
 };
-
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
 
 __global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -127,7 +131,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __gri
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
-      if (i == B_LOADED || i == B_PFULL || i == B_DQEMPTY || i == B_EPI) cnt = 256;
+      if (i == B_LOADED || i == B_PFULL || i == B_EPI) cnt = 256;
+      if (i == B_DQEMPTY || i == B_STAGED) cnt = 128;
       if (i >= B_QFULL && i < B_QFULL + NQ) cnt = 32;
       mbar_init(bar(i), cnt);
     }
@@ -143,8 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __gri
   const uint32_t tmem = *tmem_slot;
   const long long lim = p.timeout;
 
-  if (warp >= 8) {
-    regs_dec<kRegsOther>();
+  if (warp >= 8 && warp < 12) {
+    regs_dec<kRegsIssue>();
     if (warp == 8) {
       // ------------------------------------------------------------- TMA producer
       bool ok = true;
@@ -195,34 +200,54 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __gri
       __syncwarp();
     } else if (warp == 9) {
       // ------------------------------------------------------------- UMMA issuer
+      // Per query tile i, in issue order:
+      //   dV += P_i^T dO_i;  S_{i+1}^T = K Q_{i+1}^T  (commit: S ready)
+      //   dK += dS_i^T Q_i;  dQ_i = dS_i K            (commit: dQ ready)
+      //   dP_{i+1}^T = V dO_{i+1}^T, once dQ_i is read out  (commit: dP ready)
+      // so the exponentials of tile i+1 overlap dK_i and dQ_i.
       if (lane == 0) {
         constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);   // K-major x K-major
         constexpr uint32_t id_tm = idesc_bf16_f32(128, 128, 0, 1);   // tmem A x MN-major B
         constexpr uint32_t id_mm = idesc_bf16_f32(128, 128, 1, 1);   // MN-major A x MN-major B
         const uint32_t sK = sb + kOffK, sV = sb + kOffV, sDS = sb + kOffDS;
-        auto kmaj = [](uint32_t base, int kk) { return sdesc_sw128(base + (kk >> 2) * (kTile / 2) + (kk & 3) * 32, 0, 1024); };
+        auto kmaj = [](uint32_t base, int kk) {
+          return sdesc_sw128(base + (kk >> 2) * (kTile / 2) + (kk & 3) * 32, 0, 1024);
+        };
         auto mnmaj = [](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, kTile / 2, 1024); };
-        auto issue_s_dp = [&](int st) {
-          const uint32_t sQ = sb + kOffQ + st * kTile, sDO = sb + kOffDO + st * kTile;
+        auto issue_s = [&](int st) {
+          const uint32_t sQ = sb + kOffQ + st * kTile;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) umma_ss(tmem + 0, kmaj(sK, kk), kmaj(sQ, kk), id_kk, kk > 0);
+        };
+        auto issue_dp = [&](int st) {
+          const uint32_t sDO = sb + kOffDO + st * kTile;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) umma_ss(tmem + 128, kmaj(sV, kk), kmaj(sDO, kk), id_kk, kk > 0);
         };
         bool ok = mbar_wait(bar(B_KVFULL), 0, lim) && mbar_wait(bar(B_QFULL), 0, lim);
         if (ok) {
           tc_fence_after();
-          issue_s_dp(0);
+          issue_s(0);
           umma_commit(bar(B_SFULL));
+          issue_dp(0);
+          umma_commit(bar(B_DPFULL));
         }
         for (int it = 0; it < n_it && ok; ++it) {
           const int st = it % NQ;
+          const bool next = it + 1 < n_it;
+          const int st1 = (it + 1) % NQ, u1 = (it + 1) / NQ;
           const uint32_t sQ = sb + kOffQ + st * kTile, sDO = sb + kOffDO + st * kTile;
           if (!mbar_wait(bar(B_PFULL), it & 1, lim)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO
             umma_ts(tmem + 256, tmem + 0 + kk * 8, mnmaj(sDO, kk), id_tm, (it > 0 || kk > 0) ? 1u : 0u);
+          if (next) {
+            if (!mbar_wait(bar(B_QFULL + st1), u1 & 1, lim)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(st1);
+            umma_commit(bar(B_SFULL));
+          }
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q
             umma_ts(tmem + 384, tmem + 128 + kk * 8, mnmaj(sQ, kk), id_tm, (it > 0 || kk > 0) ? 1u : 0u);
@@ -230,14 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __gri
           for (int kk = 0; kk < 8; ++kk)  // dQ tile = dS K
             umma_ss(tmem + 128, mnmaj(sDS, kk), mnmaj(sK, kk), id_mm, kk > 0);
           umma_commit(bar(B_DQFULL));
-          umma_commit(bar(B_QEMPTY + st));
-          if (it + 1 < n_it) {
-            const int st1 = (it + 1) % NQ, u1 = (it + 1) / NQ;
-            if (!mbar_wait(bar(B_QFULL + st1), u1 & 1, lim)) { ok = false; break; }
+          if (next) {
             if (!mbar_wait(bar(B_DQEMPTY), it & 1, lim)) { ok = false; break; }
             tc_fence_after();
-            issue_s_dp(st1);
-            umma_commit(bar(B_SFULL));
+            issue_dp(st1);
+            umma_commit(bar(B_DPFULL));
           }
         }
         if (ok)
@@ -249,6 +271,64 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __gri
       }
       __syncwarp();
     }
+  } else if (warp >= 12) {
+    regs_dec<kRegsDq>();
+    // --------------------------------------------------------------- dQ warpgroup
+    // Row qi of the dQ tile (TMEM lane) goes, scaled by s, into the consumed
+    // Q/dO stage as four 128x32 fp32 boxes (128-byte swizzled); one thread
+    // then adds them into the fp32 accumulator with TMA reduce-add.
+    const int quarter = warp & 3;
+    const int rq = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it % NQ;
+      const int m = qr.x + it % nm;
+      const int hq = hk * p.group + it / nm;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DQFULL), it & 1, lim));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t g[32];
+        tmem_ld32(tmem + lane_base + 128 + 32 * q, g);
+        tmem_ld_wait();
+        if (q == 3) {
+          tc_fence_before();
+          mbar_arrive(bar(B_DQEMPTY));
+        }
+        // box q: columns [32q, 32q+32); Q stage holds boxes 0-1, dO stage boxes 2-3
+        const uint32_t box = (q < 2 ? sb + kOffQ + st * kTile : sb + kOffDO + st * kTile) + (q & 1) * (kTile / 2);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t addr = box + sw128_offset(rq, c);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                       "f"(p.scale * __uint_as_float(g[4 * c])), "f"(p.scale * __uint_as_float(g[4 * c + 1])),
+                       "f"(p.scale * __uint_as_float(g[4 * c + 2])), "f"(p.scale * __uint_as_float(g[4 * c + 3]))
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(B_STAGED));
+      if (rq == 0) {
+        if (mbar_wait(bar(B_STAGED), it & 1, lim)) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t box = (q < 2 ? sb + kOffQ + st * kTile : sb + kOffDO + st * kTile) + (q & 1) * (kTile / 2);
+            tma_reduce_add_4d(&p.tdq[rl], box, 32 * q, hq, b, m * 128);
+          }
+          bulk_commit();
+          bulk_wait_read_all();
+          mbar_arrive(bar(B_QEMPTY + st));
+        } else {
+          ok = false;
+        }
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+    }
+    if (rq == 0) bulk_wait_all();
+    if (!ok && lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
   } else {
     regs_inc<kRegsCompute>();
     // --------------------------------------------------------------- compute warps
@@ -268,42 +348,48 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __gri
     for (int it = 0; it < n_it; ++it) {
       const int st = it % NQ;
       const int m = qr.x + it % nm;
-      const int hq = hk * p.group + it / nm;
       ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), it & 1, lim) &&
                                        mbar_wait(bar(B_QFULL + st), (it / NQ) & 1, lim));
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[64], dp[64];
-      tmem_ld32(tmem + lane_base + 0 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-      tmem_ld32(tmem + lane_base + 32 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      uint32_t pf[64];
+      tmem_ld32(tmem + lane_base + 0 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pf[0]));
+      tmem_ld32(tmem + lane_base + 32 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pf[32]));
+      tmem_ld_wait();
+      const float* rs = rows + st * 256;
+      const int i0 = m * 128 + 64 * h;           // first query of this thread's columns
+      const bool full = qlo <= i0 && i0 + 63 <= qhi;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        float pv = ex2_approx(fmaf(__uint_as_float(pf[c]), sl2, -rs[64 * h + c]));
+        if (!full) {
+          const int i = i0 + c;
+          if (i < qlo || i > qhi) pv = 0.f;
+        }
+        pf[c] = __float_as_uint(pv);
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DPFULL), it & 1, lim));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dp[64];
       tmem_ld32(tmem + lane_base + 128 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
       tmem_ld32(tmem + lane_base + 160 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
       tmem_ld_wait();
       // Both column halves must be read before either half is overwritten.
       tc_fence_before();
       mbar_arrive(bar(B_LOADED));
-      const float* rs = rows + st * 256;
-      const int i0 = m * 128 + 64 * h;           // first query of this thread's columns
-      const bool full = qlo <= i0 && i0 + 63 <= qhi;
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float pv = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -rs[64 * h + c]));
-        if (!full) {
-          const int i = i0 + c;
-          if (i < qlo || i > qhi) pv = 0.f;
-        }
-        const float ds = pv * (__uint_as_float(dp[c]) - rs[128 + 64 * h + c]);
-        s[c] = __float_as_uint(pv);
-        dp[c] = __float_as_uint(ds);
-      }
       uint32_t pk[32], dk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        pk[c] = pack_bf16x2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1]));
-        dk[c] = pack_bf16x2(__uint_as_float(dp[2 * c]), __uint_as_float(dp[2 * c + 1]));
+        const float p0 = __uint_as_float(pf[2 * c]), p1 = __uint_as_float(pf[2 * c + 1]);
+        const float d0 = p0 * (__uint_as_float(dp[2 * c]) - rs[128 + 64 * h + 2 * c]);
+        const float d1 = p1 * (__uint_as_float(dp[2 * c + 1]) - rs[128 + 64 * h + 2 * c + 1]);
+        pk[c] = pack_bf16x2(p0, p1);
+        dk[c] = pack_bf16x2(d0, d1);
       }
       // dS^T row jr, queries [64h, 64h+64): one 128-byte row of half h of the
-      // swizzled smem tile (the MN-major A operand of dQ = dS K).
+      // swizzled smem tile (the MN-major A operand of dQ = dS K). The previous
+      // dQ UMMA finished before dP^T of this tile was committed.
       const uint32_t ds_row = sb + kOffDS + h * (kTile / 2);
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -321,24 +407,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __gri
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL));
-      // dQ tile: row = query m*128 + jr (TMEM lane), columns [64h, 64h+64).
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DQFULL), it & 1, lim));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t g[64];
-      tmem_ld32(tmem + lane_base + 128 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&g[0]));
-      tmem_ld32(tmem + lane_base + 160 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&g[32]));
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(bar(B_DQEMPTY));
-      const int qi = m * 128 + jr;
-      if (qi < p.sl) {
-        float* dst = p.dq_acc[rl] + (((size_t)qi * p.bs + b) * p.Hq + hq) * 128 + 64 * h;
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          red_add_v4(dst + 4 * c, p.scale * __uint_as_float(g[4 * c]), p.scale * __uint_as_float(g[4 * c + 1]),
-                     p.scale * __uint_as_float(g[4 * c + 2]), p.scale * __uint_as_float(g[4 * c + 3]));
-      }
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DKDV), 0, lim));
     if (ok) {
@@ -559,9 +627,11 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
                 make_tmap_bf16_4d(&prm.tdk[i], dk[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
                 make_tmap_bf16_4d(&prm.tdv[i], dv[r], 128, L.Hk, L.bs, L.sl, 64, 128);
       if (!ok) return ULYSSES_ERR_CUDA;
+      if (!make_tmap_f32_4d(&prm.tdq[i], acc_base + per_rank_acc * r, 128, L.Hq, L.bs, L.sl, 32, 128,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+        return ULYSSES_ERR_CUDA;
       prm.lse[i] = lse[r];
       prm.D[i] = D_base + per_rank_D * r;
-      prm.dq_acc[i] = acc_base + per_rank_acc * r;
     }
     const long long grid = (long long)n_n * nr * L.bs * L.Hk;
     if (grid > 0x7fffffffLL) return ULYSSES_ERR_UNSUPPORTED;

@@ -46,9 +46,10 @@ inline bool make_tmap_bf16_4d(CUtensorMap* map, const void* base, uint64_t d0, u
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The same for an fp32 tensor (used for the dQ accumulator), no swizzle.
+// The same for an fp32 tensor (the dQ accumulator). With 128-byte swizzle the
+// box is 32 floats wide.
 inline bool make_tmap_f32_4d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3,
-                             uint32_t box0, uint32_t box3) {
+                             uint32_t box0, uint32_t box3, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   const cuuint64_t dims[4] = {d0, d1, d2, d3};
@@ -56,7 +57,7 @@ inline bool make_tmap_f32_4d(CUtensorMap* map, const void* base, uint64_t d0, ui
   const cuuint32_t box[4] = {box0, 1, 1, box3};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
