@@ -50,11 +50,18 @@ using namespace sm103;
 constexpr int kRanksPerLaunch = 8;
 constexpr int kThreads = 512;
 // Registers: the block launches at 128 per thread; the compute warpgroups take
-// 192, the TMA/UMMA warpgroup keeps 56, the dQ warpgroup 72:
-// 2*128*192 + 128*56 + 128*72 = 512*128.
-constexpr int kRegsCompute = 192;
+// 160, the TMA/UMMA warpgroup keeps 56, the dQ warpgroup 136 (a whole dQ row
+// in flight): 2*128*160 + 128*56 + 128*136 = 512*128.
+constexpr int kRegsLaunch = (65536 / kThreads) / 8 * 8;  // registers per thread at launch
+constexpr int kRegsCompute = 160;
 constexpr int kRegsIssue = 56;
-constexpr int kRegsDq = 72;
+constexpr int kRegsDq = 136;
+// setmaxnreg.inc may only raise and .dec only lower a warpgroup's count, and
+// the raises must be paid for by the releases.
+static_assert(kRegsCompute >= kRegsLaunch && kRegsDq >= kRegsLaunch && kRegsIssue <= kRegsLaunch,
+              "register split directions");
+static_assert(2 * 128 * kRegsCompute + 128 * kRegsIssue + 128 * kRegsDq <= kThreads * kRegsLaunch,
+              "register split must add up to the launch budget");
 constexpr int NQ = 2;                              // Q/dO pipeline stages
 constexpr uint32_t kTile = 128 * 128 * 2;          // 32 KB
 constexpr uint32_t kOffK = 0;
@@ -201,10 +208,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __gri
     } else if (warp == 9) {
       // ------------------------------------------------------------- UMMA issuer
       // Per query tile i, in issue order:
-      //   dV += P_i^T dO_i;  S_{i+1}^T = K Q_{i+1}^T  (commit: S ready)
-      //   dK += dS_i^T Q_i;  dQ_i = dS_i K            (commit: dQ ready)
+      //   dV += P_i^T dO_i and dK += dS_i^T Q_i, interleaved (two independent
+      //   accumulators keep the tensor pipe fed);
+      //   S_{i+1}^T = K Q_{i+1}^T                     (commit: S ready)
+      //   dQ_i = dS_i K                               (commit: dQ ready)
       //   dP_{i+1}^T = V dO_{i+1}^T, once dQ_i is read out  (commit: dP ready)
-      // so the exponentials of tile i+1 overlap dK_i and dQ_i.
+      // so the exponentials of tile i+1 overlap dQ_i and its readout.
       if (lane == 0) {
         constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);   // K-major x K-major
         constexpr uint32_t id_tm = idesc_bf16_f32(128, 128, 0, 1);   // tmem A x MN-major B
@@ -240,17 +249,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __gri
           if (!mbar_wait(bar(B_PFULL), it & 1, lim)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO
-            umma_ts(tmem + 256, tmem + 0 + kk * 8, mnmaj(sDO, kk), id_tm, (it > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 8; ++kk) {  // dV += P^T dO and dK += dS^T Q
+            const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+            umma_ts(tmem + 256, tmem + 0 + kk * 8, mnmaj(sDO, kk), id_tm, acc);
+            umma_ts(tmem + 384, tmem + 128 + kk * 8, mnmaj(sQ, kk), id_tm, acc);
+          }
           if (next) {
             if (!mbar_wait(bar(B_QFULL + st1), u1 & 1, lim)) { ok = false; break; }
             tc_fence_after();
             issue_s(st1);
             umma_commit(bar(B_SFULL));
           }
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q
-            umma_ts(tmem + 384, tmem + 128 + kk * 8, mnmaj(sQ, kk), id_tm, (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dQ tile = dS K
             umma_ss(tmem + 128, mnmaj(sDS, kk), mnmaj(sK, kk), id_mm, kk > 0);
@@ -272,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __gri
       __syncwarp();
     }
   } else if (warp >= 12) {
-    regs_dec<kRegsDq>();
+    regs_inc<kRegsDq>();
     // --------------------------------------------------------------- dQ warpgroup
     // Row qi of the dQ tile (TMEM lane) goes, scaled by s, into the consumed
     // Q/dO stage as four 128x32 fp32 boxes (128-byte swizzled); one thread
@@ -288,23 +297,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __gri
       ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DQFULL), it & 1, lim));
       if (!ok) break;
       tc_fence_after();
+      uint32_t g[4][32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_base + 128 + 32 * q, g[q]);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_DQEMPTY));
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        uint32_t g[32];
-        tmem_ld32(tmem + lane_base + 128 + 32 * q, g);
-        tmem_ld_wait();
-        if (q == 3) {
-          tc_fence_before();
-          mbar_arrive(bar(B_DQEMPTY));
-        }
         // box q: columns [32q, 32q+32); Q stage holds boxes 0-1, dO stage boxes 2-3
         const uint32_t box = (q < 2 ? sb + kOffQ + st * kTile : sb + kOffDO + st * kTile) + (q & 1) * (kTile / 2);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint32_t addr = box + sw128_offset(rq, c);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                       "f"(p.scale * __uint_as_float(g[4 * c])), "f"(p.scale * __uint_as_float(g[4 * c + 1])),
-                       "f"(p.scale * __uint_as_float(g[4 * c + 2])), "f"(p.scale * __uint_as_float(g[4 * c + 3]))
+                       "f"(p.scale * __uint_as_float(g[q][4 * c])), "f"(p.scale * __uint_as_float(g[q][4 * c + 1])),
+                       "f"(p.scale * __uint_as_float(g[q][4 * c + 2])), "f"(p.scale * __uint_as_float(g[q][4 * c + 3]))
                        : "memory");
         }
       }

@@ -49,6 +49,10 @@ constexpr int kRanksPerLaunch = 8;
 constexpr int kThreads = 384;
 constexpr int kRegsSoftmax = 224;
 constexpr int kRegsOther = 56;
+constexpr int kRegsLaunch = (65536 / kThreads) / 8 * 8;  // registers per thread at launch
+static_assert(kRegsSoftmax >= kRegsLaunch && kRegsOther <= kRegsLaunch, "register split directions");
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kThreads * kRegsLaunch,
+              "register split must add up to the launch budget");
 constexpr int NS = 2;                            // K/V pipeline stages
 constexpr uint32_t kTile = 128 * 128 * 2;        // one 128x128 bf16 tile
 constexpr uint32_t kOffQ = 0;                    // 2 tiles
