@@ -68,6 +68,33 @@ def exchange_bytes(w, H):
     return 2.0 * w.sl * w.bs * H * w.hs * w.elem_bytes
 
 
+KERNEL_SOURCES = {
+    "attn_bwd_sm103_kernel": "ulysses_sequence_attention_gb300/csrc/attn_bwd_sm103.cu",
+    "attn_fwd_sm103_kernel": "ulysses_sequence_attention_gb300/csrc/attn_fwd_sm103.cu",
+}
+
+
+def captured_traffic(kernel, workload):
+    """DRAM bytes per launch from the ncu summary in profiles/traffic.txt.
+
+    The figure applies only while the kernel's source is the one that was
+    captured (sha256 prefix); otherwise the traffic is unknown (None).
+    """
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = KERNEL_SOURCES.get(kernel)
+    if not os.path.exists(path) or src is None:
+        return None, None
+    digest = hashlib.sha256(open(os.path.join(ROOT, src), "rb").read()).hexdigest()[:16]
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload:
+            if parts[2] != digest or parts[3] == "null":
+                return None, None
+            return float(parts[3]), " ".join(parts[4:])
+    return None, None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -402,11 +429,13 @@ def main():
         h2s_gbs = exchange_bytes(w, w.hc) / (r["h2s_o_ms"] * 1e-3) / 1e9
         sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
         if w.backward:
-            dom = {"kernel": "ulysses_attn_bwd", "achieved": bwd_tf, "ms": r["bwd_ms"], "flops": fl_bwd}
+            dom = {"kernel": "attn_bwd_sm103_kernel", "achieved": bwd_tf, "ms": r["bwd_ms"], "flops": fl_bwd}
         else:
-            dom = {"kernel": "ulysses_attn_fwd", "achieved": fwd_tf, "ms": r["fwd_ms"], "flops": fl_fwd}
+            dom = {"kernel": "attn_fwd_sm103_kernel", "achieved": fwd_tf, "ms": r["fwd_ms"], "flops": fl_fwd}
+        traffic, traffic_how = captured_traffic(dom["kernel"], w.name)
         roof = {"bound": "tensor", "kernel": dom["kernel"], "achieved": dom["achieved"], "peak": sustained,
-                "unit": "TFLOP/s", "frac": dom["achieved"] / sustained, "traffic": None,
+                "unit": "TFLOP/s", "frac": dom["achieved"] / sustained, "traffic": traffic,
+                "traffic_source": traffic_how,
                 "peak_source": f"{src} bf16_tflops_sustained",
                 "frac_of_burst": dom["achieved"] / peaks["bf16_tflops"],
                 "algorithmic_tflop_per_launch": dom["flops"] / 1e12, "avg_launch_ms": dom["ms"]}

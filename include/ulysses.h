@@ -202,6 +202,27 @@ int ulysses_attn_bwd(ulysses_t h, const void* const* q, const void* const* k,
 int ulysses_get_status(ulysses_t h);
 
 /*
+ * ulysses_set_wait_limit — bound, in SM clock cycles, on every device-side
+ * wait of the tensor-core kernels (mbarrier waits between warps, TMA and
+ * UMMA completions). The default is 4e9 cycles (about 2 s). A wait that
+ * runs out sets the handle's status word, and the kernel winds down without
+ * touching more data; ulysses_get_status then returns ULYSSES_ERR_TIMEOUT.
+ * cycles must be positive (ULYSSES_ERR_INVALID_ARG otherwise). Host only.
+ */
+int ulysses_set_wait_limit(ulysses_t h, int64_t cycles);
+
+/*
+ * ulysses_inject_fault — test hook for the failure path; never needed in use.
+ *   kind 0: no fault (clears a pending one).
+ *   kind 1: in the next tensor-core forward call, the TMA producer issues no
+ *           K/V loads, so the waits for them run out. Combine with a short
+ *           ulysses_set_wait_limit. The injection is consumed by that call.
+ * Nothing faults, traps or hangs: every wait is bounded. Returns
+ * ULYSSES_ERR_INVALID_ARG for an unknown kind. Host only.
+ */
+int ulysses_inject_fault(ulysses_t h, int kind);
+
+/*
  * ulysses_launch_count — number of CUDA kernels this library has enqueued
  * since it was loaded, over all handles and threads. A diagnostic counter for
  * benchmarks: the difference across a region is the number of launches the

@@ -11,6 +11,6 @@ from ._binding import (  # noqa: F401
     ULYSSES_MAX_P, ULYSSES_OK, ULYSSES_NOALLOC_SCRATCH_BYTES, UlyssesError, UlyssesHandle, ulysses_attn_bwd,
     ulysses_attn_bwd_noalloc, ulysses_attn_fwd,
     ulysses_create, ulysses_destroy, ulysses_get_status, ulysses_head_to_seq, ulysses_launch_count, ulysses_seq_to_head,
-    ulysses_strerror, ulysses_workspace_size,
+    ulysses_strerror, ulysses_workspace_size, ulysses_set_wait_limit, ulysses_inject_fault,
 )
 from .layer import UlyssesLayer  # noqa: F401

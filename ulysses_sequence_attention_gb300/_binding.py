@@ -65,6 +65,10 @@ lib.ulysses_get_status.argtypes = [_vp]
 lib.ulysses_get_status.restype = ctypes.c_int
 lib.ulysses_attn_bwd_noalloc.argtypes = [_vp] + [_pp] * 9 + [_vp]
 lib.ulysses_attn_bwd_noalloc.restype = ctypes.c_int
+lib.ulysses_set_wait_limit.argtypes = [_vp, ctypes.c_int64]
+lib.ulysses_set_wait_limit.restype = ctypes.c_int
+lib.ulysses_inject_fault.argtypes = [_vp, ctypes.c_int]
+lib.ulysses_inject_fault.restype = ctypes.c_int
 lib.ulysses_launch_count.argtypes = []
 lib.ulysses_launch_count.restype = ctypes.c_uint64
 
@@ -239,3 +243,11 @@ def ulysses_attn_bwd_noalloc(h: UlyssesHandle, q, k, v, o, do, lse, dq, dk, dv, 
             _ptrs(h, lse, h.bs * h.Hq * h.sl, torch.float32, "lse"),
             _ptrs(h, dq, nq, dt, "dq"), _ptrs(h, dk, nk, dt, "dk"), _ptrs(h, dv, nk, dt, "dv")]
     _check(lib.ulysses_attn_bwd_noalloc(h.ptr, *args, _stream(stream)), "ulysses_attn_bwd_noalloc")
+
+
+def ulysses_set_wait_limit(h: UlyssesHandle, cycles: int):
+    _check(lib.ulysses_set_wait_limit(h.ptr, int(cycles)), "ulysses_set_wait_limit")
+
+
+def ulysses_inject_fault(h: UlyssesHandle, kind: int):
+    _check(lib.ulysses_inject_fault(h.ptr, int(kind)), "ulysses_inject_fault")

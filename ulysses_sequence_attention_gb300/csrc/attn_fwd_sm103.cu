@@ -73,6 +73,7 @@ struct FwdParams {
   unsigned* status;
   long long timeout;      // clock cycles per wait
   int ndoc, sl, bs, Hq, Hk, group, npairs, nranks, causal;
+  int skip_kv_loads;      // test hook: the producer issues no K/V loads
   float scale_log2;
 };
 
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103_kernel(const __gri
         tma_load_4d(dst, &p.tq[rl], bar(B_QFULL), 0, hq0 + t, b, m * 128);
         tma_load_4d(dst + kTile / 2, &p.tq[rl], bar(B_QFULL), 64, hq0 + t, b, m * 128);
       }
-      for (int jj = 0; jj < n_kv; ++jj) {
+      for (int jj = 0; jj < (p.skip_kv_loads ? 0 : n_kv); ++jj) {
         const int st = jj % NS, u = jj / NS;
         const int row = (kr.x + jj) * 128;
         if (!mbar_wait(bar(B_KEMPTY + st), (u & 1) ^ 1, lim)) { ok = false; break; }
@@ -393,7 +394,7 @@ void plan_tiles(const Layer& L, std::vector<int2>& kv_range, std::vector<int>& o
 
 bool fwd_sm103_supported(const Layer& L) { return L.dtype == ULYSSES_BF16 && L.hs == 128; }
 
-int launch_attn_fwd_sm103(const Layer& L, const void* const* q, const void* const* k, const void* const* v,
+int launch_attn_fwd_sm103(Layer& L, const void* const* q, const void* const* k, const void* const* v,
                           void* const* o, float* const* lse, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
@@ -418,6 +419,8 @@ int launch_attn_fwd_sm103(const Layer& L, const void* const* q, const void* cons
   prm.group = group;
   prm.npairs = (group + 1) / 2;
   prm.causal = L.causal;
+  prm.skip_kv_loads = L.inject_fault == 1 ? 1 : 0;
+  L.inject_fault = 0;
   prm.scale_log2 = (float)(1.4426950408889634 / sqrt((double)L.hs));
   for (int r0 = 0; r0 < L.P; r0 += kRanksPerLaunch) {
     const int nr = std::min(kRanksPerLaunch, L.P - r0);

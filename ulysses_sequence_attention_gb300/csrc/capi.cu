@@ -207,7 +207,7 @@ int ulysses_head_to_seq(ulysses_t h, int nheads, const void* const* head_shards,
 
 int ulysses_attn_fwd(ulysses_t h, const void* const* q, const void* const* k,
                      const void* const* v, void* const* o, float* const* lse, void* stream) {
-  const Layer* L = reinterpret_cast<const Layer*>(h);
+  Layer* L = reinterpret_cast<Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
   if (L->empty()) return ULYSSES_OK;
   CHECK_PTRS(q);
@@ -242,6 +242,20 @@ int ulysses_attn_bwd(ulysses_t h, const void* const* q, const void* const* k,
     return uly::launch_attn_bwd_sm103(*L, q, k, v, o, dO, lse, dq, dk, dv, workspace, (cudaStream_t)stream);
   return uly::launch_attn_bwd_simt(*L, q, k, v, o, dO, lse, dq, dk, dv, workspace,
                                    (cudaStream_t)stream);
+}
+
+int ulysses_set_wait_limit(ulysses_t h, int64_t cycles) {
+  Layer* L = reinterpret_cast<Layer*>(h);
+  if (!L || cycles <= 0) return ULYSSES_ERR_INVALID_ARG;
+  L->timeout_cycles = cycles;
+  return ULYSSES_OK;
+}
+
+int ulysses_inject_fault(ulysses_t h, int kind) {
+  Layer* L = reinterpret_cast<Layer*>(h);
+  if (!L || kind < 0 || kind > 1) return ULYSSES_ERR_INVALID_ARG;
+  L->inject_fault = kind;
+  return ULYSSES_OK;
 }
 
 uint64_t ulysses_launch_count(void) { return uly::g_launches.load(std::memory_order_relaxed); }

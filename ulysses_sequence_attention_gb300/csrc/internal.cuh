@@ -33,6 +33,7 @@ struct Layer {
   int2* d_q_range = nullptr;
   int* d_n_order = nullptr;
   long long timeout_cycles = 4000000000LL;  // bound of every device-side wait (~2 s)
+  int inject_fault = 0;                     // test hook (ulysses_inject_fault)
   int64_t n() const { return sl / P; }          // tokens per sequence shard
   int esize() const { return dtype == ULYSSES_BF16 ? 2 : 4; }
   bool empty() const { return sl == 0 || bs == 0; }
@@ -79,7 +80,7 @@ int launch_attn_bwd_simt(const Layer& L, const void* const* q, const void* const
 
 bool fwd_sm103_supported(const Layer& L);
 void plan_tiles(const Layer& L, std::vector<int2>& kv_range, std::vector<int>& order);
-int launch_attn_fwd_sm103(const Layer& L, const void* const* q, const void* const* k, const void* const* v,
+int launch_attn_fwd_sm103(Layer& L, const void* const* q, const void* const* k, const void* const* v,
                           void* const* o, float* const* lse, cudaStream_t s);
 
 void plan_bwd_tiles(const Layer& L, std::vector<int2>& q_range, std::vector<int>& order);
