@@ -112,9 +112,8 @@ const char* ulysses_strerror(int status);
 
 /*
  * ulysses_workspace_size — bytes of device workspace that ulysses_attn_bwd needs.
- * Layout: for each rank, an fp32 dQ accumulator [sl][bs][hc/P][hs], then for
- * each rank an fp32 D = rowsum(dO * O) array [bs][hc/P][sl]. Pure host
- * computation.
+ * Layout: for each rank, the fp32 rows D = rowsum(dO * O), [bs][hc/P][sl]
+ * (P * bs * hc * sl * 4 bytes in all). Pure host computation.
  */
 int ulysses_workspace_size(ulysses_t h, size_t* bytes);
 
@@ -254,8 +253,9 @@ uint64_t ulysses_launch_count(void);
  * Limits and sharing:
  *  - A layer whose backward needs more than ULYSSES_NOALLOC_SCRATCH_BYTES of
  *    workspace (see ulysses_workspace_size) is rejected with
- *    ULYSSES_ERR_TOO_LARGE before anything is enqueued. For the Llama-8B head
- *    shape (32 query heads, head size 128, bf16) that allows about 4K tokens.
+ *    ULYSSES_ERR_TOO_LARGE before anything is enqueued. The workspace is 4
+ *    bytes per (token, query head, batch element): 64 MiB covers, for example,
+ *    512K tokens of a 32-query-head layer.
  *  - Every call shares the one array, and it keeps the last call's contents.
  *    Each call clears the parts that must start at zero itself. Two calls that
  *    overlap on the GPU (on different streams, or different host threads

@@ -1,4 +1,4 @@
-// attn_bwd_sm103.cu — attention backward on the tcgen05 tensor cores.
+// attn_bwd_sm103.cu — attention backward on the tcgen05 tensor cores, two SMs per tile.
 //
 // The backward of the layer reverses its forward (HF blog "Ulysses Sequence
 // Parallelism: Training with Million-Token Contexts", algorithm steps 3-5):
@@ -8,31 +8,31 @@
 //   dQ_i = s sum_j dS_ij k_j,  dK_j = s sum_i dS_ij q_i
 // and the kv gradients of a GQA group sum over its query heads.
 //
-// Three kernels:
-//  1. bwd_prep: D = rowsum(dO * O) in fp32, and the fp32 dQ accumulator set to zero.
-//  2. bwd_main: one CTA per (rank, batch, kv head, 128-key tile). It keeps K and
-//     V in shared memory and loops over every query head of the group and every
-//     128-row query tile that can see the keys (causal and per-document block
-//     skipping). Per query tile the tensor core computes
-//        S^T = K Q^T,  dP^T = V dO^T                      (into tensor memory)
-//        dV += P^T dO,  dK += dS^T Q                      (accumulated in tensor memory)
-//        dQ_tile = dS K                                   (into tensor memory)
-//     and eight compute warps turn S^T, dP^T into P^T and dS^T (bf16) between
-//     the two halves. A fourth warpgroup reads each dQ tile out of tensor
-//     memory, stages it in the consumed Q/dO stage and adds it into the fp32
-//     accumulator with TMA reduce-add (whole 128-byte lines at L2). At the end
-//     dK (scaled by s) and dV leave by TMA store.
-//  3. bwd_dq_convert: dQ = bf16(accumulator).
+// Three kernels, no atomics:
+//  1. bwd_prep: D = rowsum(dO * O) in fp32.
+//  2. bwd_dkdv: a CTA pair owns 256 keys (128 per CTA) of one kv head. For every
+//     query head of the group and every 128-row query tile that can see the keys
+//     (causal and per-document block skipping), the pair computes with M = 256
+//     UMMAs (tcgen05 .cta_group::2, issued by the even CTA):
+//        S^T = K Q^T,  dP^T = V dO^T                 (tensor memory)
+//        dV += P^T dO,  dK += dS^T Q                 (accumulated in tensor memory)
+//     and eight compute warps per CTA turn S^T, dP^T into P^T, dS^T (bf16),
+//     both written over dP^T, so that S^T of the next tile can be issued
+//     while dV and dK of this one still run. At the end dK (times s) and dV
+//     leave by TMA store.
+//  3. bwd_dq: a CTA pair owns 256 queries of one query head and loops over the
+//     visible key tiles:
+//        S = Q K^T,  dP = dO V^T,  dQ += dS K        (M = 256 UMMAs)
+//     with dS written in place over dP as the tensor-memory A operand.
+// Recomputing S and dP for dQ costs two more GEMMs per tile than accumulating
+// dQ with atomics, but M = 256 UMMAs run at about twice the rate of the M = 128
+// form, and dQ needs no fp32 reduction traffic.
 //
-// Tensor memory: [0,128) S^T, then P^T (bf16) in [0,64); [128,256) dP^T, then
-// dS^T (bf16) in [128,192), then the dQ tile; [256,384) dV; [384,512) dK.
-// Reuse relies on UMMAs from one thread running in issue order.
-//
-// Warp roles (512 threads): warps 0-7 compute (thread = kv row / TMEM lane,
-// warp w handles columns [64*(w/4), 64*(w/4)+64)); warp 8 TMA and the LSE/D
-// rows; warp 9 UMMA and tensor-memory allocation; warps 10-11 complete the
-// third warpgroup; warps 12-15 move the dQ tiles. Every mbarrier wait is
-// bounded.
+// In a pair, the B operand of each UMMA is split along N: for N = queries (or
+// keys) each CTA holds 64 of the 128 rows; for N = head dimension each CTA
+// holds 64 of its 128 columns. TMA loads of the odd CTA complete on its own
+// barriers and are forwarded to the even CTA's barriers with a remote arrive.
+// Every mbarrier wait is bounded.
 #include <math.h>
 
 #include <algorithm>
@@ -48,43 +48,29 @@ namespace {
 using namespace sm103;
 
 constexpr int kRanksPerLaunch = 8;
-constexpr int kThreads = 512;
-// Registers: the block launches at 128 per thread; the compute warpgroups take
-// 160, the TMA/UMMA warpgroup keeps 56, the dQ warpgroup 136 (a whole dQ row
-// in flight): 2*128*160 + 128*56 + 128*136 = 512*128.
+constexpr int kThreads = 384;
 constexpr int kRegsLaunch = (65536 / kThreads) / 8 * 8;  // registers per thread at launch
-constexpr int kRegsCompute = 160;
-constexpr int kRegsIssue = 56;
-constexpr int kRegsDq = 136;
-// setmaxnreg.inc may only raise and .dec only lower a warpgroup's count, and
-// the raises must be paid for by the releases.
-static_assert(kRegsCompute >= kRegsLaunch && kRegsDq >= kRegsLaunch && kRegsIssue <= kRegsLaunch,
-              "register split directions");
-static_assert(2 * 128 * kRegsCompute + 128 * kRegsIssue + 128 * kRegsDq <= kThreads * kRegsLaunch,
+constexpr int kRegsCompute = 224;
+constexpr int kRegsOther = 56;
+static_assert(kRegsCompute >= kRegsLaunch && kRegsOther <= kRegsLaunch, "register split directions");
+static_assert(2 * 128 * kRegsCompute + 128 * kRegsOther <= kThreads * kRegsLaunch,
               "register split must add up to the launch budget");
-constexpr int NQ = 2;                              // Q/dO pipeline stages
-constexpr uint32_t kTile = 128 * 128 * 2;          // 32 KB
-constexpr uint32_t kOffK = 0;
-constexpr uint32_t kOffV = kTile;
-constexpr uint32_t kOffQ = 2 * kTile;              // NQ tiles
-constexpr uint32_t kOffDO = kOffQ + NQ * kTile;    // NQ tiles
-constexpr uint32_t kOffDS = kOffDO + NQ * kTile;   // 1 tile
-constexpr uint32_t kOffRow = kOffDS + kTile;       // NQ x (128 LSE + 128 D) floats
-constexpr uint32_t kOffBar = kOffRow + NQ * 1024;
-constexpr uint32_t kSmemBytes = kOffBar + 256;     // the dynamic base must be 1024-aligned
+constexpr uint32_t kTile = 128 * 128 * 2;  // a 128x128 bf16 tile: 32 KB
+constexpr uint32_t kHalf = kTile / 2;      // 16 KB
 
-struct BwdParams {
-  CUtensorMap tq[kRanksPerLaunch];
-  CUtensorMap tk[kRanksPerLaunch];
-  CUtensorMap tv[kRanksPerLaunch];
-  CUtensorMap tdo[kRanksPerLaunch];
-  CUtensorMap tdk[kRanksPerLaunch];
-  CUtensorMap tdv[kRanksPerLaunch];
-  CUtensorMap tdq[kRanksPerLaunch];    // fp32 accumulator [sl][bs][Hq][128], boxes of 32 x 128
+struct PairParams {
+  CUtensorMap ta[kRanksPerLaunch];   // dkdv: K 64x128     dq: Q 64x128
+  CUtensorMap tb[kRanksPerLaunch];   // dkdv: V 64x128     dq: dO 64x128
+  CUtensorMap tc[kRanksPerLaunch];   // dkdv: Q 64x64      dq: K 64x64
+  CUtensorMap td[kRanksPerLaunch];   // dkdv: dO 64x64     dq: V 64x64
+  CUtensorMap te[kRanksPerLaunch];   // dkdv: Q 64x128     dq: K 64x128
+  CUtensorMap tf[kRanksPerLaunch];   // dkdv: dO 64x128    dq: dQ (store)
+  CUtensorMap tg[kRanksPerLaunch];   // dkdv: dK (store)
+  CUtensorMap th[kRanksPerLaunch];   // dkdv: dV (store)
   const float* lse[kRanksPerLaunch];
-  const float* D[kRanksPerLaunch];     // [bs][Hq][sl]
-  const int2* q_range;                 // per key tile: first and last query tile
-  const int* n_order;                  // key tiles, most work first
+  const float* D[kRanksPerLaunch];   // [bs][Hq][sl]
+  const int2* range;                 // per pair tile: first and last tile of the other side
+  const int* order;                  // pair tiles, most work first
   const int32_t* doc_offsets;
   unsigned* status;
   long long timeout;
@@ -92,259 +78,287 @@ struct BwdParams {
   float scale, scale_log2;
 };
 
-enum {
-  B_KVFULL = 0,
-  B_QFULL = 1,                 // NQ: Q, dO tiles and their LSE/D rows (32 arrivals + tx)
-  B_QEMPTY = B_QFULL + NQ,     // NQ: the stage's dQ reduction has read it (1)
-  B_SFULL = B_QEMPTY + NQ,     // S^T done (commit)
-  B_DPFULL = B_SFULL + 1,      // dP^T done (commit)
-  B_LOADED = B_DPFULL + 1,     // compute warps hold S^T, dP^T in registers (256)
-  B_PFULL = B_LOADED + 1,      // P^T, dS^T written (256)
-  B_DQFULL = B_PFULL + 1,      // dQ tile done (commit)
-  B_DQEMPTY = B_DQFULL + 1,    // dQ tile read out of tensor memory (128)
-  B_STAGED = B_DQEMPTY + 1,    // dQ tile staged in shared memory (128)
-  B_DKDV = B_STAGED + 1,       // every UMMA done (commit)
-  B_EPI = B_DKDV + 1,          // dK/dV staged (256)
-  B_DRAIN = B_EPI + 1,
-  B_COUNT
-};
+__device__ __forceinline__ void pair_status(const PairParams& p) { atomicOr(p.status, STATUS_TIMEOUT); }
 
-__global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __grid_constant__ BwdParams p) {
+// Per-warp arrival on a barrier of the even CTA (remote from the odd one).
+__device__ __forceinline__ void warp_arrive_leader(uint32_t bar_local, uint32_t crank) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    if (crank == 0)
+      mbar_arrive(bar_local);
+    else
+      mbar_arrive_cluster(mapa(bar_local, 0));
+  }
+}
+__device__ __forceinline__ void warp_arrive_local(uint32_t bar_local) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar_local);
+}
+
+// Stage a thread's row of a 128-row x 64-column bf16 block (64 values as 32
+// packed words), 128-byte swizzled, at `region`.
+__device__ __forceinline__ void stage_row64(uint32_t region, int row, const uint32_t (&w)[32]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t addr = region + sw128_offset(row, c);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * c]), "r"(w[4 * c + 1]),
+                 "r"(w[4 * c + 2]), "r"(w[4 * c + 3])
+                 : "memory");
+  }
+}
+
+// ===========================================================================
+// dK / dV: pair = 256 keys
+// ===========================================================================
+namespace dkdv {
+constexpr int NQ = 2;
+constexpr uint32_t kOffK = 0, kOffV = kTile;
+// Per stage: Qn, dOn (this CTA's 64 query rows x 128, K-major), then Qh, dOh
+// (all 128 query rows x this CTA's 64 head columns, MN-major).
+constexpr uint32_t kOffStage = 2 * kTile;
+constexpr uint32_t kStage = 4 * kHalf;
+constexpr int NR = 4;                                  // LSE/D row ring
+constexpr uint32_t kOffRow = kOffStage + NQ * kStage;  // NR x (128 LSE + 128 D) floats
+constexpr uint32_t kOffBar = kOffRow + NR * 1024;
+constexpr uint32_t kSmem = kOffBar + 256;
+enum {
+  B_KV = 0,                  // K, V landed (even CTA: + the odd CTA's forward)
+  B_QFULL = 1,               // NQ: query-half part (Qn, dOn) landed (even CTA: + 1 forward)
+  B_QEMPTY = B_QFULL + NQ,   // NQ: query-half part consumed by S^T, dP^T (commit, both CTAs)
+  B_HFULL = B_QEMPTY + NQ,   // NQ: head-half part (Qh, dOh) landed (even CTA: + 1 forward)
+  B_HEMPTY = B_HFULL + NQ,   // NQ: head-half part consumed by dV, dK (commit, both)
+  B_S = B_HEMPTY + NQ,       // S^T ready (commit, both)
+  B_DP = B_S + 1,            // dP^T ready (commit, both)
+  B_LOADED = B_DP + 1,       // this CTA's compute warps hold S^T, dP^T (8 warps)
+  B_P = B_LOADED + 1,        // even CTA: P^T, dS^T written in both CTAs (16 warps)
+  B_DONE = B_P + 1,          // every UMMA done (commit, both)
+  B_EPI = B_DONE + 1,        // dK, dV staged (8 warps)
+  B_DRAIN = B_EPI + 1,
+  B_RFULL = B_DRAIN + 1,     // NR: LSE/D rows written (32 lanes, this CTA)
+  B_REMPTY = B_RFULL + NR,   // NR: rows read by this CTA's compute warps (8 warps)
+  B_COUNT = B_REMPTY + NR
+};
+}  // namespace dkdv
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ PairParams p) {
+  using namespace dkdv;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
-  if (sb & 1023u) {  // the layout needs a 1024-byte aligned base; report instead of misreading
-    if (threadIdx.x == 0) atomicOr(p.status, STATUS_TIMEOUT);
+  if (sb & 1023u) {  // same condition in both CTAs: both leave before any cluster barrier
+    if (threadIdx.x == 0) pair_status(p);
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * B_COUNT);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  float* rows = reinterpret_cast<float*>(smem + kOffRow);  // [NQ][2][128]: LSE*log2(e), D
-
+  float* rows = reinterpret_cast<float*>(smem + kOffRow);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_rank();
 
-  // Work item: (key tile, rank, batch, kv head).
+  // Pair work item: (key pair tile, rank, batch, kv head).
+  const int pair = blockIdx.x >> 1;
   const int units = p.nranks * p.bs * p.Hk;
-  const int n = p.n_order[blockIdx.x / units];
-  int rest = blockIdx.x % units;
+  const int np = p.order[pair / units];
+  int rest = pair % units;
   const int hk = rest % p.Hk;
   rest /= p.Hk;
   const int b = rest % p.bs;
   const int rl = rest / p.bs;
-  const int2 qr = p.q_range[n];
+  const int2 qr = p.range[np];
   const int nm = qr.y - qr.x + 1;
   const int n_it = p.group * nm;
+  const int kv0 = np * 256 + 128 * (int)crank;  // this CTA's first key
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
-      if (i == B_LOADED || i == B_PFULL || i == B_EPI) cnt = 256;
-      if (i == B_DQEMPTY || i == B_STAGED) cnt = 128;
-      if (i >= B_QFULL && i < B_QFULL + NQ) cnt = 32;
+      if (i == B_KV || (i >= B_HFULL && i < B_HFULL + NQ) || (i >= B_QFULL && i < B_QFULL + NQ))
+        cnt = crank == 0 ? 2 : 1;
+      if (i >= B_RFULL && i < B_RFULL + NR) cnt = 32;
+      if (i == B_LOADED || i == B_EPI || (i >= B_REMPTY && i < B_REMPTY + NR)) cnt = 8;
+      if (i == B_P) cnt = 16;
       mbar_init(bar(i), cnt);
     }
     fence_mbar_init();
   }
   if (warp == 9) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
+    tmem_alloc2(smem_u32(tmem_slot), 512);
+    tmem_relinquish2();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // barriers of both CTAs exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const long long lim = p.timeout;
 
-  if (warp >= 8 && warp < 12) {
-    regs_dec<kRegsIssue>();
+  if (warp >= 8) {
+    regs_dec<kRegsOther>();
     if (warp == 8) {
-      // ------------------------------------------------------------- TMA producer
+      // --------------------------------------------------------- TMA producer
       bool ok = true;
-      int last_q[NQ];
-      for (int i = 0; i < NQ; ++i) last_q[i] = -1;
+      int last[NQ], last_h[NQ];
+      for (int i = 0; i < NQ; ++i) last[i] = last_h[i] = -1;
       if (lane == 0) {
-        mbar_expect_tx(bar(B_KVFULL), 2 * kTile);
-        tma_load_4d(sb + kOffK, &p.tk[rl], bar(B_KVFULL), 0, hk, b, n * 128);
-        tma_load_4d(sb + kOffK + kTile / 2, &p.tk[rl], bar(B_KVFULL), 64, hk, b, n * 128);
-        tma_load_4d(sb + kOffV, &p.tv[rl], bar(B_KVFULL), 0, hk, b, n * 128);
-        tma_load_4d(sb + kOffV + kTile / 2, &p.tv[rl], bar(B_KVFULL), 64, hk, b, n * 128);
+        mbar_expect_tx(bar(B_KV), 2 * kTile);
+        tma_load_4d(sb + kOffK, &p.ta[rl], bar(B_KV), 0, hk, b, kv0);
+        tma_load_4d(sb + kOffK + kHalf, &p.ta[rl], bar(B_KV), 64, hk, b, kv0);
+        tma_load_4d(sb + kOffV, &p.tb[rl], bar(B_KV), 0, hk, b, kv0);
+        tma_load_4d(sb + kOffV + kHalf, &p.tb[rl], bar(B_KV), 64, hk, b, kv0);
       }
       for (int it = 0; it < n_it; ++it) {
         const int st = it % NQ, u = it / NQ;
         const int hq = hk * p.group + it / nm;
         const int m = qr.x + it % nm;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QEMPTY + st), (u & 1) ^ 1, lim));
+        const uint32_t sq = sb + kOffStage + st * kStage;
+        const int q0 = m * 128;
+        // LSE (log2 units) and D rows of the tile; rows past the end get
+        // LSE = +inf, so that P = 0 there.
+        const int rsl = it % NR;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_REMPTY + rsl), ((it / NR) & 1) ^ 1, lim));
         if (!ok) break;
-        // LSE (in log2 units) and D of the tile's 128 rows; rows past the end
-        // get LSE = +inf, so that P = 0 there.
-        float* rs = rows + st * 256;
+        float* rs = rows + rsl * 256;
         const size_t base = ((size_t)b * p.Hq + hq) * p.sl;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int i = m * 128 + lane * 4 + e;
+          const int i = q0 + lane * 4 + e;
           const bool in = i < p.sl;
           rs[lane * 4 + e] = in ? p.lse[rl][base + i] * 1.4426950408889634f : INFINITY;
           rs[128 + lane * 4 + e] = in ? p.D[rl][base + i] : 0.f;
         }
+        mbar_arrive(bar(B_RFULL + rsl));
+        // query-half part: Q and dO rows [q0 + 64c, +64) (B of S^T, dP^T: N = queries)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QEMPTY + st), (u & 1) ^ 1, lim));
+        if (!ok) break;
         if (lane == 0) {
-          mbar_expect_tx(bar(B_QFULL + st), 2 * kTile);
-          const uint32_t dq = sb + kOffQ + st * kTile, ddo = sb + kOffDO + st * kTile;
-          tma_load_4d(dq, &p.tq[rl], bar(B_QFULL + st), 0, hq, b, m * 128);
-          tma_load_4d(dq + kTile / 2, &p.tq[rl], bar(B_QFULL + st), 64, hq, b, m * 128);
-          tma_load_4d(ddo, &p.tdo[rl], bar(B_QFULL + st), 0, hq, b, m * 128);
-          tma_load_4d(ddo + kTile / 2, &p.tdo[rl], bar(B_QFULL + st), 64, hq, b, m * 128);
-        } else {
-          mbar_arrive(bar(B_QFULL + st));
+          const int qh = q0 + 64 * (int)crank;
+          mbar_expect_tx(bar(B_QFULL + st), 2 * kHalf);
+          tma_load_4d(sq, &p.tc[rl], bar(B_QFULL + st), 0, hq, b, qh);
+          tma_load_4d(sq + kHalf / 2, &p.tc[rl], bar(B_QFULL + st), 64, hq, b, qh);
+          tma_load_4d(sq + kHalf, &p.td[rl], bar(B_QFULL + st), 0, hq, b, qh);
+          tma_load_4d(sq + kHalf + kHalf / 2, &p.td[rl], bar(B_QFULL + st), 64, hq, b, qh);
         }
-        last_q[st] = u;
+        last[st] = u;
+        // head-half part: Q and dO columns [64c, 64c+64) of all 128 rows (B of dK, dV)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_HEMPTY + st), (u & 1) ^ 1, lim));
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_expect_tx(bar(B_HFULL + st), 2 * kHalf);
+          tma_load_4d(sq + 2 * kHalf, &p.te[rl], bar(B_HFULL + st), 64 * (int)crank, hq, b, q0);
+          tma_load_4d(sq + 3 * kHalf, &p.tf[rl], bar(B_HFULL + st), 64 * (int)crank, hq, b, q0);
+        }
+        last_h[st] = u;
       }
       if (lane == 0) {
-        if (!ok) atomicOr(p.status, STATUS_TIMEOUT);
-        mbar_wait(bar(B_KVFULL), 0, lim);
-        for (int i = 0; i < NQ; ++i)
-          if (last_q[i] >= 0) mbar_wait(bar(B_QFULL + i), last_q[i] & 1, lim);
+        if (!ok) pair_status(p);
+        mbar_wait(bar(B_KV), 0, lim);
+        for (int i = 0; i < NQ; ++i) {
+          if (last[i] >= 0) mbar_wait(bar(B_QFULL + i), last[i] & 1, lim);
+          if (last_h[i] >= 0) mbar_wait(bar(B_HFULL + i), last_h[i] & 1, lim);
+        }
       }
       __syncwarp();
-    } else if (warp == 9) {
-      // ------------------------------------------------------------- UMMA issuer
-      // Per query tile i, in issue order:
-      //   dV += P_i^T dO_i and dK += dS_i^T Q_i, interleaved (two independent
-      //   accumulators keep the tensor pipe fed);
-      //   S_{i+1}^T = K Q_{i+1}^T                     (commit: S ready)
-      //   dQ_i = dS_i K                               (commit: dQ ready)
-      //   dP_{i+1}^T = V dO_{i+1}^T, once dQ_i is read out  (commit: dP ready)
-      // so the exponentials of tile i+1 overlap dQ_i and its readout.
+    } else if (warp == 9 && crank == 0) {
+      // --------------------------------------------------------- UMMA issuer (even CTA)
       if (lane == 0) {
-        constexpr uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);   // K-major x K-major
-        constexpr uint32_t id_tm = idesc_bf16_f32(128, 128, 0, 1);   // tmem A x MN-major B
-        constexpr uint32_t id_mm = idesc_bf16_f32(128, 128, 1, 1);   // MN-major A x MN-major B
-        const uint32_t sK = sb + kOffK, sV = sb + kOffV, sDS = sb + kOffDS;
-        auto kmaj = [](uint32_t base, int kk) {
-          return sdesc_sw128(base + (kk >> 2) * (kTile / 2) + (kk & 3) * 32, 0, 1024);
+        constexpr uint32_t id_kk = idesc_bf16_f32(256, 128, 0, 0);
+        constexpr uint32_t id_tm = idesc_bf16_f32(256, 128, 0, 1);
+        const uint32_t sK = sb + kOffK, sV = sb + kOffV;
+        auto a_kmaj = [](uint32_t base, int kk) {  // 128 rows, K = 128
+          return sdesc_sw128(base + (kk >> 2) * kHalf + (kk & 3) * 32, 0, 1024);
         };
-        auto mnmaj = [](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, kTile / 2, 1024); };
+        auto b_kmaj64 = [](uint32_t base, int kk) {  // 64 rows, K = 128
+          return sdesc_sw128(base + (kk >> 2) * (kHalf / 2) + (kk & 3) * 32, 0, 1024);
+        };
+        auto b_mn = [](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, kHalf, 1024); };
         auto issue_s = [&](int st) {
-          const uint32_t sQ = sb + kOffQ + st * kTile;
+          const uint32_t sq = sb + kOffStage + st * kStage;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) umma_ss(tmem + 0, kmaj(sK, kk), kmaj(sQ, kk), id_kk, kk > 0);
+          for (int kk = 0; kk < 8; ++kk) umma2_ss(tmem + 0, a_kmaj(sK, kk), b_kmaj64(sq, kk), id_kk, kk > 0);
         };
         auto issue_dp = [&](int st) {
-          const uint32_t sDO = sb + kOffDO + st * kTile;
+          const uint32_t sq = sb + kOffStage + st * kStage;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) umma_ss(tmem + 128, kmaj(sV, kk), kmaj(sDO, kk), id_kk, kk > 0);
+          for (int kk = 0; kk < 8; ++kk)
+            umma2_ss(tmem + 128, a_kmaj(sV, kk), b_kmaj64(sq + kHalf, kk), id_kk, kk > 0);
         };
-        bool ok = mbar_wait(bar(B_KVFULL), 0, lim) && mbar_wait(bar(B_QFULL), 0, lim);
+        bool ok = mbar_wait(bar(B_KV), 0, lim) && mbar_wait(bar(B_QFULL), 0, lim);
         if (ok) {
           tc_fence_after();
           issue_s(0);
-          umma_commit(bar(B_SFULL));
+          umma2_commit_both(bar(B_S));
           issue_dp(0);
-          umma_commit(bar(B_DPFULL));
+          umma2_commit_both(bar(B_DP));
+          umma2_commit_both(bar(B_QEMPTY));
         }
+        // Per query tile i, in issue order:
+        //   S_{i+1}^T (its columns were read before P_i was signalled), then
+        //   dV += P_i^T dO_i and dK += dS_i^T Q_i interleaved, then
+        //   dP_{i+1}^T (over P_i^T and dS_i^T, after dV and dK have read them).
+        // The exponentials of tile i+1 overlap dV_i and dK_i.
         for (int it = 0; it < n_it && ok; ++it) {
           const int st = it % NQ;
           const bool next = it + 1 < n_it;
           const int st1 = (it + 1) % NQ, u1 = (it + 1) / NQ;
-          const uint32_t sQ = sb + kOffQ + st * kTile, sDO = sb + kOffDO + st * kTile;
-          if (!mbar_wait(bar(B_PFULL), it & 1, lim)) { ok = false; break; }
+          const uint32_t sq = sb + kOffStage + st * kStage;
+          if (!mbar_wait(bar(B_P), it & 1, lim)) { ok = false; break; }
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // dV += P^T dO and dK += dS^T Q
-            const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-            umma_ts(tmem + 256, tmem + 0 + kk * 8, mnmaj(sDO, kk), id_tm, acc);
-            umma_ts(tmem + 384, tmem + 128 + kk * 8, mnmaj(sQ, kk), id_tm, acc);
-          }
           if (next) {
             if (!mbar_wait(bar(B_QFULL + st1), u1 & 1, lim)) { ok = false; break; }
             tc_fence_after();
             issue_s(st1);
-            umma_commit(bar(B_SFULL));
+            umma2_commit_both(bar(B_S));
           }
+          if (!mbar_wait(bar(B_HFULL + st), (it / NQ) & 1, lim)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dQ tile = dS K
-            umma_ss(tmem + 128, mnmaj(sDS, kk), mnmaj(sK, kk), id_mm, kk > 0);
-          umma_commit(bar(B_DQFULL));
+          for (int kk = 0; kk < 8; ++kk) {  // dV += P^T dO and dK += dS^T Q, interleaved
+            const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+            umma2_ts(tmem + 256, tmem + 192 + kk * 8, b_mn(sq + 3 * kHalf, kk), id_tm, acc);
+            umma2_ts(tmem + 384, tmem + 128 + kk * 8, b_mn(sq + 2 * kHalf, kk), id_tm, acc);
+          }
+          umma2_commit_both(bar(B_HEMPTY + st));
           if (next) {
-            if (!mbar_wait(bar(B_DQEMPTY), it & 1, lim)) { ok = false; break; }
-            tc_fence_after();
-            issue_dp(st1);
-            umma_commit(bar(B_DPFULL));
+            issue_dp(st1);  // overwrites P^T and dS^T only after dV and dK have read them
+            umma2_commit_both(bar(B_DP));
+            umma2_commit_both(bar(B_QEMPTY + st1));  // the query part of tile it+1 is consumed
           }
         }
         if (ok)
-          umma_commit(bar(B_DKDV));
+          umma2_commit_both(bar(B_DONE));
         else
-          atomicOr(p.status, STATUS_TIMEOUT);
-        umma_commit(bar(B_DRAIN));
+          pair_status(p);
+        umma2_commit_both(bar(B_DRAIN));
         mbar_wait(bar(B_DRAIN), 0, lim);
       }
       __syncwarp();
-    }
-  } else if (warp >= 12) {
-    regs_inc<kRegsDq>();
-    // --------------------------------------------------------------- dQ warpgroup
-    // Row qi of the dQ tile (TMEM lane) goes, scaled by s, into the consumed
-    // Q/dO stage as four 128x32 fp32 boxes (128-byte swizzled); one thread
-    // then adds them into the fp32 accumulator with TMA reduce-add.
-    const int quarter = warp & 3;
-    const int rq = quarter * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int st = it % NQ;
-      const int m = qr.x + it % nm;
-      const int hq = hk * p.group + it / nm;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DQFULL), it & 1, lim));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t g[4][32];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_base + 128 + 32 * q, g[q]);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(bar(B_DQEMPTY));
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        // box q: columns [32q, 32q+32); Q stage holds boxes 0-1, dO stage boxes 2-3
-        const uint32_t box = (q < 2 ? sb + kOffQ + st * kTile : sb + kOffDO + st * kTile) + (q & 1) * (kTile / 2);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t addr = box + sw128_offset(rq, c);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                       "f"(p.scale * __uint_as_float(g[q][4 * c])), "f"(p.scale * __uint_as_float(g[q][4 * c + 1])),
-                       "f"(p.scale * __uint_as_float(g[q][4 * c + 2])), "f"(p.scale * __uint_as_float(g[q][4 * c + 3]))
-                       : "memory");
+    } else if (warp == 10 && crank == 1) {
+      // --------------------------------------------------------- forwarder (odd CTA)
+      // The even CTA's UMMAs read this CTA's shared memory: tell it when the
+      // loads have landed.
+      if (lane == 0) {
+        bool ok = mbar_wait(bar(B_KV), 0, lim);
+        if (ok) mbar_arrive_cluster(mapa(bar(B_KV), 0));
+        for (int it = 0; it < n_it && ok; ++it) {
+          const int st = it % NQ, u = it / NQ;
+          ok = mbar_wait(bar(B_QFULL + st), u & 1, lim);
+          if (ok) mbar_arrive_cluster(mapa(bar(B_QFULL + st), 0));
+          if (ok) ok = mbar_wait(bar(B_HFULL + st), u & 1, lim);
+          if (ok) mbar_arrive_cluster(mapa(bar(B_HFULL + st), 0));
         }
+        if (!ok) pair_status(p);
       }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(B_STAGED));
-      if (rq == 0) {
-        if (mbar_wait(bar(B_STAGED), it & 1, lim)) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t box = (q < 2 ? sb + kOffQ + st * kTile : sb + kOffDO + st * kTile) + (q & 1) * (kTile / 2);
-            tma_reduce_add_4d(&p.tdq[rl], box, 32 * q, hq, b, m * 128);
-          }
-          bulk_commit();
-          bulk_wait_read_all();
-          mbar_arrive(bar(B_QEMPTY + st));
-        } else {
-          ok = false;
-        }
-      }
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
+      __syncwarp();
     }
-    if (rq == 0) bulk_wait_all();
-    if (!ok && lane == 0) atomicOr(p.status, STATUS_TIMEOUT);
   } else {
     regs_inc<kRegsCompute>();
-    // --------------------------------------------------------------- compute warps
+    // ----------------------------------------------------------- compute warps
     const int quarter = warp & 3;
-    const int h = warp >> 2;                   // column half
-    const int jr = quarter * 32 + lane;        // kv row within the tile = TMEM lane
-    const int j = n * 128 + jr;                // global key position
-    int qlo = 1, qhi = 0;                      // queries that see key j: [qlo, qhi]
+    const int h = warp >> 2;                 // query half: columns [64h, 64h+64)
+    const int jr = quarter * 32 + lane;      // key row within this CTA = TMEM lane
+    const int j = kv0 + jr;                  // global key position
+    int qlo = 1, qhi = 0;                    // queries that see key j: [qlo, qhi]
     if (j < p.sl) {
       const int d = doc_of(p.doc_offsets, p.ndoc, j);
       qlo = p.causal ? j : p.doc_offsets[d];
@@ -354,18 +368,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __gri
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
-      const int st = it % NQ;
       const int m = qr.x + it % nm;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL), it & 1, lim) &&
-                                       mbar_wait(bar(B_QFULL + st), (it / NQ) & 1, lim));
+      const int rsl = it % NR;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_S), it & 1, lim) &&
+                                       mbar_wait(bar(B_RFULL + rsl), (it / NR) & 1, lim));
       if (!ok) break;
       tc_fence_after();
       uint32_t pf[64];
       tmem_ld32(tmem + lane_base + 0 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pf[0]));
       tmem_ld32(tmem + lane_base + 32 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pf[32]));
       tmem_ld_wait();
-      const float* rs = rows + st * 256;
-      const int i0 = m * 128 + 64 * h;           // first query of this thread's columns
+      const float* rs = rows + rsl * 256;
+      const int i0 = m * 128 + 64 * h;
       const bool full = qlo <= i0 && i0 + 63 <= qhi;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
@@ -376,16 +390,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __gri
         }
         pf[c] = __float_as_uint(pv);
       }
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DPFULL), it & 1, lim));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DP), it & 1, lim));
       if (!ok) break;
       tc_fence_after();
       uint32_t dp[64];
       tmem_ld32(tmem + lane_base + 128 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
       tmem_ld32(tmem + lane_base + 160 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
       tmem_ld_wait();
-      // Both column halves must be read before either half is overwritten.
       tc_fence_before();
-      mbar_arrive(bar(B_LOADED));
+      warp_arrive_local(bar(B_LOADED));  // both halves read before either is overwritten
       uint32_t pk[32], dk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
@@ -395,100 +408,367 @@ __global__ void __launch_bounds__(kThreads, 1) attn_bwd_sm103_kernel(const __gri
         pk[c] = pack_bf16x2(p0, p1);
         dk[c] = pack_bf16x2(d0, d1);
       }
-      // dS^T row jr, queries [64h, 64h+64): one 128-byte row of half h of the
-      // swizzled smem tile (the MN-major A operand of dQ = dS K). The previous
-      // dQ UMMA finished before dP^T of this tile was committed.
-      const uint32_t ds_row = sb + kOffDS + h * (kTile / 2);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t addr = ds_row + sw128_offset(jr, c);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(dk[4 * c]), "r"(dk[4 * c + 1]),
-                     "r"(dk[4 * c + 2]), "r"(dk[4 * c + 3])
-                     : "memory");
-      }
+      warp_arrive_local(bar(B_REMPTY + rsl));  // done with this tile's LSE/D rows
       ok = __all_sync(0xffffffffu, mbar_wait(bar(B_LOADED), it & 1, lim));
       if (!ok) break;
       tc_fence_after();
-      tmem_st32(tmem + lane_base + 0 + 32 * h, pk);      // P^T, bf16
-      tmem_st32(tmem + lane_base + 128 + 32 * h, dk);    // dS^T, bf16
+      tmem_st32(tmem + lane_base + 192 + 32 * h, pk);  // P^T (bf16), over dP^T
+      tmem_st32(tmem + lane_base + 128 + 32 * h, dk);  // dS^T (bf16), over dP^T
       tmem_st_wait();
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(B_PFULL));
+      warp_arrive_leader(bar(B_P), crank);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DKDV), 0, lim));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DONE), 0, lim));
     if (ok) {
       tc_fence_after();
-      // dV (cols 256+) and dK (cols 384+, times s) of kv row jr, columns [64h,64h+64),
-      // staged into the V and K tiles (free now) and stored by TMA.
+      // dV (columns 256+) and dK (384+, times s) of key row jr, head-dimension
+      // half h, staged in this CTA's V and K tiles (free now) and TMA-stored.
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const float mul = which == 0 ? 1.f : p.scale;
         const uint32_t col = (which == 0 ? 256 : 384) + 64 * h;
-        const uint32_t stage = sb + (which == 0 ? kOffV : kOffK) + h * (kTile / 2);
+        uint32_t o[64], w[32];
+        tmem_ld32(tmem + lane_base + col, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+        tmem_ld32(tmem + lane_base + col + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+        tmem_ld_wait();
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_base + col + 32 * q, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(o[c4 * 8 + 2 * e]) * mul, __uint_as_float(o[c4 * 8 + 2 * e + 1]) * mul);
-            const uint32_t addr = stage + sw128_offset(jr, q * 4 + c4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                         "r"(w[3])
-                         : "memory");
-          }
-        }
+        for (int c = 0; c < 32; ++c)
+          w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * mul, __uint_as_float(o[2 * c + 1]) * mul);
+        stage_row64(sb + (which == 0 ? kOffV : kOffK) + h * kHalf, jr, w);
       }
       fence_proxy_async_smem();
-      mbar_arrive(bar(B_EPI));
+      warp_arrive_local(bar(B_EPI));
       if (threadIdx.x == 0) {
         if (mbar_wait(bar(B_EPI), 0, lim)) {
-          tma_store_4d(&p.tdv[rl], sb + kOffV, 0, hk, b, n * 128);
-          tma_store_4d(&p.tdv[rl], sb + kOffV + kTile / 2, 64, hk, b, n * 128);
-          tma_store_4d(&p.tdk[rl], sb + kOffK, 0, hk, b, n * 128);
-          tma_store_4d(&p.tdk[rl], sb + kOffK + kTile / 2, 64, hk, b, n * 128);
+          tma_store_4d(&p.th[rl], sb + kOffV, 0, hk, b, kv0);
+          tma_store_4d(&p.th[rl], sb + kOffV + kHalf, 64, hk, b, kv0);
+          tma_store_4d(&p.tg[rl], sb + kOffK, 0, hk, b, kv0);
+          tma_store_4d(&p.tg[rl], sb + kOffK + kHalf, 64, hk, b, kv0);
           bulk_commit();
           bulk_wait_all();
         } else {
-          atomicOr(p.status, STATUS_TIMEOUT);
+          pair_status(p);
         }
       }
     } else if (lane == 0) {
-      atomicOr(p.status, STATUS_TIMEOUT);
+      pair_status(p);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // no remote arrive or multicast commit can target an exited CTA
   if (warp == 9) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc2(tmem, 512);
   }
 }
 
-// D = rowsum(dO * O) for every (rank, batch, head, row), and dq_acc = 0.
-// Eight lanes per row, 16 bytes of O and of dO per lane.
+// ===========================================================================
+// dQ: pair = 256 queries
+// ===========================================================================
+namespace dqk {
+constexpr int NK = 3;
+constexpr uint32_t kOffQ = 0, kOffDO = kTile;
+// Per stage: Kn, Vn (this CTA's 64 key rows x 128, K-major), then Kh (all 128
+// key rows x this CTA's 64 head columns, MN-major).
+constexpr uint32_t kOffStage = 2 * kTile;
+constexpr uint32_t kStage = 3 * kHalf;
+constexpr uint32_t kOffBar = kOffStage + NK * kStage;
+constexpr uint32_t kSmem = kOffBar + 256;
+enum {
+  B_QO = 0,                  // Q, dO landed (even CTA: + forward)
+  B_KFULL = 1,               // NK: key stage landed (even CTA: + forward)
+  B_KEMPTY = B_KFULL + NK,   // NK: key stage consumed (commit, both)
+  B_S = B_KEMPTY + NK,       // 2: S ready in buffer 0 / 1 (commit, both)
+  B_DP = B_S + 2,            // dP ready (commit, both)
+  B_LOADED = B_DP + 1,       // this CTA's compute warps hold dP (8 warps)
+  B_DS = B_LOADED + 1,       // even CTA: dS written in both CTAs (16 warps)
+  B_DONE = B_DS + 1,         // every UMMA done (commit, both)
+  B_EPI = B_DONE + 1,        // dQ staged (8 warps)
+  B_DRAIN = B_EPI + 1,
+  B_COUNT
+};
+}  // namespace dqk
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ PairParams p) {
+  using namespace dqk;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sb = smem_u32(smem);
+  if (sb & 1023u) {
+    if (threadIdx.x == 0) pair_status(p);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * B_COUNT);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_rank();
+
+  // Pair work item: (query pair tile, rank, batch, query head).
+  const int pair = blockIdx.x >> 1;
+  const int units = p.nranks * p.bs * p.Hq;
+  const int mp = p.order[pair / units];
+  int rest = pair % units;
+  const int hq = rest % p.Hq;
+  rest /= p.Hq;
+  const int b = rest % p.bs;
+  const int rl = rest / p.bs;
+  const int hk = hq / p.group;
+  const int2 kr = p.range[mp];
+  const int n_kv = kr.y - kr.x + 1;
+  const int q0 = mp * 256 + 128 * (int)crank;  // this CTA's first query
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < B_COUNT; ++i) {
+      uint32_t cnt = 1;
+      if (i == B_QO || (i >= B_KFULL && i < B_KFULL + NK)) cnt = crank == 0 ? 2 : 1;
+      if (i == B_LOADED || i == B_EPI) cnt = 8;
+      if (i == B_DS) cnt = 16;
+      mbar_init(bar(i), cnt);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc2(smem_u32(tmem_slot), 512);
+    tmem_relinquish2();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const long long lim = p.timeout;
+  // Tensor memory: S in [0,128) and [128,256) (two buffers), dP in [256,384)
+  // with dS (bf16) written over [256,320), the dQ accumulator in [384,512).
+
+  if (warp >= 8) {
+    regs_dec<kRegsOther>();
+    if (warp == 8) {
+      // --------------------------------------------------------- TMA producer
+      if (lane == 0) {
+        bool ok = true;
+        int last[NK];
+        for (int i = 0; i < NK; ++i) last[i] = -1;
+        mbar_expect_tx(bar(B_QO), 2 * kTile);
+        tma_load_4d(sb + kOffQ, &p.ta[rl], bar(B_QO), 0, hq, b, q0);
+        tma_load_4d(sb + kOffQ + kHalf, &p.ta[rl], bar(B_QO), 64, hq, b, q0);
+        tma_load_4d(sb + kOffDO, &p.tb[rl], bar(B_QO), 0, hq, b, q0);
+        tma_load_4d(sb + kOffDO + kHalf, &p.tb[rl], bar(B_QO), 64, hq, b, q0);
+        for (int jj = 0; jj < n_kv; ++jj) {
+          const int st = jj % NK, u = jj / NK;
+          const int k0 = (kr.x + jj) * 128;
+          const int kh = k0 + 64 * (int)crank;
+          if (!mbar_wait(bar(B_KEMPTY + st), (u & 1) ^ 1, lim)) { ok = false; break; }
+          const uint32_t sk = sb + kOffStage + st * kStage;
+          mbar_expect_tx(bar(B_KFULL + st), 3 * kHalf);
+          // key half of K and V (B of S, dP: N = keys)
+          tma_load_4d(sk, &p.tc[rl], bar(B_KFULL + st), 0, hk, b, kh);
+          tma_load_4d(sk + kHalf / 2, &p.tc[rl], bar(B_KFULL + st), 64, hk, b, kh);
+          tma_load_4d(sk + kHalf, &p.td[rl], bar(B_KFULL + st), 0, hk, b, kh);
+          tma_load_4d(sk + kHalf + kHalf / 2, &p.td[rl], bar(B_KFULL + st), 64, hk, b, kh);
+          // head-dimension half of K (B of dQ: N = head dimension)
+          tma_load_4d(sk + 2 * kHalf, &p.te[rl], bar(B_KFULL + st), 64 * (int)crank, hk, b, k0);
+          last[st] = u;
+        }
+        if (!ok) pair_status(p);
+        mbar_wait(bar(B_QO), 0, lim);
+        for (int i = 0; i < NK; ++i)
+          if (last[i] >= 0) mbar_wait(bar(B_KFULL + i), last[i] & 1, lim);
+      }
+      __syncwarp();
+    } else if (warp == 9 && crank == 0) {
+      // --------------------------------------------------------- UMMA issuer (even CTA)
+      if (lane == 0) {
+        constexpr uint32_t id_kk = idesc_bf16_f32(256, 128, 0, 0);
+        constexpr uint32_t id_tm = idesc_bf16_f32(256, 128, 0, 1);
+        const uint32_t sQ = sb + kOffQ, sDO = sb + kOffDO;
+        auto a_kmaj = [](uint32_t base, int kk) {
+          return sdesc_sw128(base + (kk >> 2) * kHalf + (kk & 3) * 32, 0, 1024);
+        };
+        auto b_kmaj64 = [](uint32_t base, int kk) {
+          return sdesc_sw128(base + (kk >> 2) * (kHalf / 2) + (kk & 3) * 32, 0, 1024);
+        };
+        auto b_mn = [](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, kHalf, 1024); };
+        auto issue_s = [&](int jj) {
+          const uint32_t sk = sb + kOffStage + (jj % NK) * kStage;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma2_ss(tmem + (jj & 1) * 128, a_kmaj(sQ, kk), b_kmaj64(sk, kk), id_kk, kk > 0);
+          umma2_commit_both(bar(B_S + (jj & 1)));
+        };
+        auto issue_dp = [&](int jj) {
+          const uint32_t sk = sb + kOffStage + (jj % NK) * kStage;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma2_ss(tmem + 256, a_kmaj(sDO, kk), b_kmaj64(sk + kHalf, kk), id_kk, kk > 0);
+          umma2_commit_both(bar(B_DP));
+        };
+        bool ok = mbar_wait(bar(B_QO), 0, lim) && mbar_wait(bar(B_KFULL), 0, lim);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+          issue_dp(0);
+        }
+        for (int jj = 0; jj < n_kv && ok; ++jj) {
+          const int st = jj % NK;
+          const bool next = jj + 1 < n_kv;
+          if (next) {
+            const int st1 = (jj + 1) % NK, u1 = (jj + 1) / NK;
+            if (!mbar_wait(bar(B_KFULL + st1), u1 & 1, lim)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(jj + 1);  // the other S buffer: its last reader finished before dS of jj-1
+          }
+          if (!mbar_wait(bar(B_DS), jj & 1, lim)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sk = sb + kOffStage + st * kStage;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // dQ += dS K
+            umma2_ts(tmem + 384, tmem + 256 + kk * 8, b_mn(sk + 2 * kHalf, kk), id_tm, (jj > 0 || kk > 0) ? 1u : 0u);
+          umma2_commit_both(bar(B_KEMPTY + st));
+          if (next) issue_dp(jj + 1);  // overwrites dS only after dQ has read it (issue order)
+        }
+        if (ok)
+          umma2_commit_both(bar(B_DONE));
+        else
+          pair_status(p);
+        umma2_commit_both(bar(B_DRAIN));
+        mbar_wait(bar(B_DRAIN), 0, lim);
+      }
+      __syncwarp();
+    } else if (warp == 10 && crank == 1) {
+      // --------------------------------------------------------- forwarder (odd CTA)
+      if (lane == 0) {
+        bool ok = mbar_wait(bar(B_QO), 0, lim);
+        if (ok) mbar_arrive_cluster(mapa(bar(B_QO), 0));
+        for (int jj = 0; jj < n_kv && ok; ++jj) {
+          const int st = jj % NK, u = jj / NK;
+          ok = mbar_wait(bar(B_KFULL + st), u & 1, lim);
+          if (ok) mbar_arrive_cluster(mapa(bar(B_KFULL + st), 0));
+        }
+        if (!ok) pair_status(p);
+      }
+      __syncwarp();
+    }
+  } else {
+    regs_inc<kRegsCompute>();
+    // ----------------------------------------------------------- compute warps
+    const int quarter = warp & 3;
+    const int h = warp >> 2;                 // key half: columns [64h, 64h+64)
+    const int iq = quarter * 32 + lane;      // query row within this CTA = TMEM lane
+    const int i = q0 + iq;                   // global query position
+    int klo = 1, khi = 0;                    // keys visible from query i: [klo, khi]
+    float lse2 = INFINITY, Di = 0.f;
+    if (i < p.sl) {
+      const int d = doc_of(p.doc_offsets, p.ndoc, i);
+      klo = p.doc_offsets[d];
+      khi = p.causal ? i : p.doc_offsets[d + 1] - 1;
+      const size_t base = ((size_t)b * p.Hq + hq) * p.sl + i;
+      lse2 = p.lse[rl][base] * 1.4426950408889634f;
+      Di = p.D[rl][base];
+    }
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int jj = 0; jj < n_kv; ++jj) {
+      const int k0 = (kr.x + jj) * 128 + 64 * h;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_S + (jj & 1)), (jj >> 1) & 1, lim));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t pf[64];
+      const uint32_t scol = (jj & 1) * 128 + 64 * h;
+      tmem_ld32(tmem + lane_base + scol, *reinterpret_cast<uint32_t(*)[32]>(&pf[0]));
+      tmem_ld32(tmem + lane_base + scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&pf[32]));
+      tmem_ld_wait();
+      const bool full = klo <= k0 && k0 + 63 <= khi;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        float pv = ex2_approx(fmaf(__uint_as_float(pf[c]), sl2, -lse2));
+        if (!full) {
+          const int key = k0 + c;
+          if (key < klo || key > khi) pv = 0.f;
+        }
+        pf[c] = __float_as_uint(pv);
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DP), jj & 1, lim));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dp[64];
+      tmem_ld32(tmem + lane_base + 256 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+      tmem_ld32(tmem + lane_base + 288 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      warp_arrive_local(bar(B_LOADED));
+      uint32_t dk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float d0 = __uint_as_float(pf[2 * c]) * (__uint_as_float(dp[2 * c]) - Di);
+        const float d1 = __uint_as_float(pf[2 * c + 1]) * (__uint_as_float(dp[2 * c + 1]) - Di);
+        dk[c] = pack_bf16x2(d0, d1);
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_LOADED), jj & 1, lim));
+      if (!ok) break;
+      tc_fence_after();
+      tmem_st32(tmem + lane_base + 256 + 32 * h, dk);  // dS (bf16) over dP
+      tmem_st_wait();
+      tc_fence_before();
+      warp_arrive_leader(bar(B_DS), crank);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DONE), 0, lim));
+    if (ok) {
+      tc_fence_after();
+      // dQ (times s) of query row iq, head-dimension half h, staged in the Q
+      // tile (free now) and TMA-stored.
+      uint32_t o[64], w[32];
+      tmem_ld32(tmem + lane_base + 384 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+      tmem_ld32(tmem + lane_base + 416 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * p.scale, __uint_as_float(o[2 * c + 1]) * p.scale);
+      stage_row64(sb + kOffQ + h * kHalf, iq, w);
+      fence_proxy_async_smem();
+      warp_arrive_local(bar(B_EPI));
+      if (threadIdx.x == 0) {
+        if (mbar_wait(bar(B_EPI), 0, lim)) {
+          tma_store_4d(&p.tf[rl], sb + kOffQ, 0, hq, b, q0);
+          tma_store_4d(&p.tf[rl], sb + kOffQ + kHalf, 64, hq, b, q0);
+          bulk_commit();
+          bulk_wait_all();
+        } else {
+          pair_status(p);
+        }
+      }
+    } else if (lane == 0) {
+      pair_status(p);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc2(tmem, 512);
+  }
+}
+
+// D = rowsum(dO * O) for every (rank, batch, head, row). 16 lanes per row.
 struct PrepParams {
   const __nv_bfloat16* o[ULYSSES_MAX_P];
   const __nv_bfloat16* dO[ULYSSES_MAX_P];
   float* D[ULYSSES_MAX_P];
-  float4* dq_acc[ULYSSES_MAX_P];
   int P, sl, bs, Hq;
-  long long rows_per_rank;      // sl * bs * Hq
-  long long acc_vec_per_rank;   // sl * bs * Hq * 32
+  long long rows_per_rank;  // sl * bs * Hq
 };
 
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constant__ PrepParams a) {
   const long long total_rows = a.rows_per_rank * a.P;
   const long long nthreads = (long long)gridDim.x * blockDim.x;
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  // 16 threads per row: 8 bf16 of O and of dO each. The loop runs whole
-  // warps (the shuffle below needs every lane); lanes past the end add zeros.
+  // The loop runs whole warps (the shuffle below needs every lane); lanes
+  // past the end add zeros.
   const long long lane = threadIdx.x & 31;
   for (long long g = tid; g - lane < total_rows * 16; g += nthreads) {
     const bool active = g < total_rows * 16;
@@ -519,54 +799,44 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constan
       a.D[r][((long long)bb * a.Hq + hq) * a.sl + t] = acc;
     }
   }
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (long long g = tid; g < a.acc_vec_per_rank * a.P; g += nthreads) {
-    const int r = (int)(g / a.acc_vec_per_rank);
-    a.dq_acc[r][g - (long long)r * a.acc_vec_per_rank] = z;
-  }
-}
-
-struct ConvParams {
-  const float4* acc[ULYSSES_MAX_P];
-  __nv_bfloat16* dq[ULYSSES_MAX_P];
-  int P;
-  long long vec_per_rank;
-};
-
-__global__ void __launch_bounds__(256) attn_bwd_dq_convert_kernel(const __grid_constant__ ConvParams a) {
-  const long long nthreads = (long long)gridDim.x * blockDim.x;
-  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < a.vec_per_rank * a.P; g += nthreads) {
-    const int r = (int)(g / a.vec_per_rank);
-    const long long e = g - (long long)r * a.vec_per_rank;
-    const float4 v = a.acc[r][e];
-    uint2 out;
-    out.x = pack_bf16x2(v.x, v.y);
-    out.y = pack_bf16x2(v.z, v.w);
-    reinterpret_cast<uint2*>(a.dq[r])[e] = out;
-  }
 }
 
 }  // namespace
 
-void plan_bwd_tiles(const Layer& L, std::vector<int2>& q_range, std::vector<int>& order) {
+// Pair schedules. dK/dV: per 256-key pair tile, the range of 128-row query
+// tiles that can see any of its keys. dQ: per 256-query pair tile, the range
+// of 128-row key tiles any of its queries can see. Both ordered by work.
+void plan_bwd_tiles(const Layer& L, std::vector<int2>& kv_pairs, std::vector<int>& kv_order,
+                    std::vector<int2>& q_pairs, std::vector<int>& q_order) {
   const int sl = (int)L.sl;
-  const int n_n = (sl + 127) / 128;
-  q_range.resize(n_n);
-  std::vector<int> cost(n_n);
+  const int n_pair = (sl + 255) / 256;
   auto doc = [&](int t) {
     return (int)(std::upper_bound(L.doc_offsets.begin(), L.doc_offsets.end(), t) - L.doc_offsets.begin()) - 1;
   };
-  for (int n = 0; n < n_n; ++n) {
-    const int first = n * 128, last = std::min(sl, first + 128) - 1;
+  auto order_by = [](const std::vector<int2>& r, std::vector<int>& order) {
+    order.resize(r.size());
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int a, int c) { return r[a].y - r[a].x > r[c].y - r[c].x; });
+  };
+  kv_pairs.resize(n_pair);
+  q_pairs.resize(n_pair);
+  for (int t = 0; t < n_pair; ++t) {
+    const int first = t * 256, last = std::min(sl, first + 256) - 1;
+    // keys [first, last]: the queries that see them
     const int lo_q = L.causal ? first : L.doc_offsets[doc(first)];
     const int hi_q = L.doc_offsets[doc(last) + 1] - 1;
-    q_range[n] = make_int2(lo_q / 128, hi_q / 128);
-    cost[n] = q_range[n].y - q_range[n].x + 1;
+    kv_pairs[t] = make_int2(lo_q / 128, hi_q / 128);
+    // queries [first, last]: the keys they see
+    const int lo_k = L.doc_offsets[doc(first)];
+    const int hi_k = L.causal ? last : L.doc_offsets[doc(last) + 1] - 1;
+    q_pairs[t] = make_int2(lo_k / 128, hi_k / 128);
   }
-  order.resize(n_n);
-  std::iota(order.begin(), order.end(), 0);
-  std::stable_sort(order.begin(), order.end(), [&](int a, int c) { return cost[a] > cost[c]; });
+  order_by(kv_pairs, kv_order);
+  order_by(q_pairs, q_order);
 }
+
+size_t bwd_sm103_workspace(const Layer& L) { return (size_t)L.P * L.bs * L.Hq * L.sl * sizeof(float); }
 
 static int grid_cap(long long work) {
   long long g = (work + 255) / 256;
@@ -578,38 +848,33 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
                           void* const* dk, void* const* dv, void* workspace, cudaStream_t stream) {
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_bwd_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dkdv::kSmem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dqk::kSmem) !=
+            cudaSuccess)
       return ULYSSES_ERR_CUDA;
     attr_set = true;
   }
-  const long long per_rank_acc = (long long)L.sl * L.bs * L.Hq * L.hs;  // floats
-  float* acc_base = reinterpret_cast<float*>(workspace);
-  float* D_base = acc_base + per_rank_acc * L.P;
+  float* D_base = reinterpret_cast<float*>(workspace);
   const long long per_rank_D = (long long)L.bs * L.Hq * L.sl;
 
-  // 1. D and zeroed accumulators.
+  // 1. D = rowsum(dO * O).
   {
     PrepParams a;
     for (int r = 0; r < L.P; ++r) {
       a.o[r] = reinterpret_cast<const __nv_bfloat16*>(o[r]);
       a.dO[r] = reinterpret_cast<const __nv_bfloat16*>(dO[r]);
       a.D[r] = D_base + per_rank_D * r;
-      a.dq_acc[r] = reinterpret_cast<float4*>(acc_base + per_rank_acc * r);
     }
     a.P = L.P;
     a.sl = (int)L.sl;
     a.bs = (int)L.bs;
     a.Hq = L.Hq;
     a.rows_per_rank = (long long)L.sl * L.bs * L.Hq;
-    a.acc_vec_per_rank = per_rank_acc / 4;
     attn_bwd_prep_kernel<<<grid_cap(a.rows_per_rank * L.P * 16), 256, 0, stream>>>(a);
     count_launches(1);
   }
-  // 2. Main kernel, in launches of up to kRanksPerLaunch ranks.
-  BwdParams prm;
-  prm.q_range = L.d_q_range;
-  prm.n_order = L.d_n_order;
+  PairParams prm;
   prm.doc_offsets = L.d_doc_offsets;
   prm.status = L.d_status;
   prm.timeout = L.timeout_cycles;
@@ -622,41 +887,44 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
   prm.causal = L.causal;
   prm.scale = (float)(1.0 / sqrt((double)L.hs));
   prm.scale_log2 = (float)(1.4426950408889634 / sqrt((double)L.hs));
-  const int n_n = (int)((L.sl + 127) / 128);
-  for (int r0 = 0; r0 < L.P; r0 += kRanksPerLaunch) {
-    const int nr = std::min(kRanksPerLaunch, L.P - r0);
-    prm.nranks = nr;
-    for (int i = 0; i < nr; ++i) {
-      const int r = r0 + i;
-      bool ok = make_tmap_bf16_4d(&prm.tq[i], q[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
-                make_tmap_bf16_4d(&prm.tk[i], k[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
-                make_tmap_bf16_4d(&prm.tv[i], v[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
-                make_tmap_bf16_4d(&prm.tdo[i], dO[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
-                make_tmap_bf16_4d(&prm.tdk[i], dk[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
-                make_tmap_bf16_4d(&prm.tdv[i], dv[r], 128, L.Hk, L.bs, L.sl, 64, 128);
-      if (!ok) return ULYSSES_ERR_CUDA;
-      if (!make_tmap_f32_4d(&prm.tdq[i], acc_base + per_rank_acc * r, 128, L.Hq, L.bs, L.sl, 32, 128,
-                            CU_TENSOR_MAP_SWIZZLE_128B))
-        return ULYSSES_ERR_CUDA;
-      prm.lse[i] = lse[r];
-      prm.D[i] = D_base + per_rank_D * r;
+  const int n_pair = (int)((L.sl + 255) / 256);
+  for (int pass = 0; pass < 2; ++pass) {  // 2. dK, dV   3. dQ
+    prm.range = pass == 0 ? L.d_kvp_range : L.d_qp_range;
+    prm.order = pass == 0 ? L.d_kvp_order : L.d_qp_order;
+    for (int r0 = 0; r0 < L.P; r0 += kRanksPerLaunch) {
+      const int nr = std::min(kRanksPerLaunch, L.P - r0);
+      prm.nranks = nr;
+      for (int i = 0; i < nr; ++i) {
+        const int r = r0 + i;
+        bool ok;
+        if (pass == 0)
+          ok = make_tmap_bf16_4d(&prm.ta[i], k[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
+               make_tmap_bf16_4d(&prm.tb[i], v[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
+               make_tmap_bf16_4d(&prm.tc[i], q[r], 128, L.Hq, L.bs, L.sl, 64, 64) &&
+               make_tmap_bf16_4d(&prm.td[i], dO[r], 128, L.Hq, L.bs, L.sl, 64, 64) &&
+               make_tmap_bf16_4d(&prm.te[i], q[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
+               make_tmap_bf16_4d(&prm.tf[i], dO[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
+               make_tmap_bf16_4d(&prm.tg[i], dk[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
+               make_tmap_bf16_4d(&prm.th[i], dv[r], 128, L.Hk, L.bs, L.sl, 64, 128);
+        else
+          ok = make_tmap_bf16_4d(&prm.ta[i], q[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
+               make_tmap_bf16_4d(&prm.tb[i], dO[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
+               make_tmap_bf16_4d(&prm.tc[i], k[r], 128, L.Hk, L.bs, L.sl, 64, 64) &&
+               make_tmap_bf16_4d(&prm.td[i], v[r], 128, L.Hk, L.bs, L.sl, 64, 64) &&
+               make_tmap_bf16_4d(&prm.te[i], k[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
+               make_tmap_bf16_4d(&prm.tf[i], dq[r], 128, L.Hq, L.bs, L.sl, 64, 128);
+        if (!ok) return ULYSSES_ERR_CUDA;
+        prm.lse[i] = lse[r];
+        prm.D[i] = D_base + per_rank_D * r;
+      }
+      const long long pairs = (long long)n_pair * nr * L.bs * (pass == 0 ? L.Hk : L.Hq);
+      if (2 * pairs > 0x7fffffffLL) return ULYSSES_ERR_UNSUPPORTED;
+      if (pass == 0)
+        attn_bwd_dkdv_kernel<<<(unsigned)(2 * pairs), kThreads, dkdv::kSmem, stream>>>(prm);
+      else
+        attn_bwd_dq_kernel<<<(unsigned)(2 * pairs), kThreads, dqk::kSmem, stream>>>(prm);
+      count_launches(1);
     }
-    const long long grid = (long long)n_n * nr * L.bs * L.Hk;
-    if (grid > 0x7fffffffLL) return ULYSSES_ERR_UNSUPPORTED;
-    attn_bwd_sm103_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(prm);
-    count_launches(1);
-  }
-  // 3. dQ to bf16.
-  {
-    ConvParams a;
-    for (int r = 0; r < L.P; ++r) {
-      a.acc[r] = reinterpret_cast<const float4*>(acc_base + per_rank_acc * r);
-      a.dq[r] = reinterpret_cast<__nv_bfloat16*>(dq[r]);
-    }
-    a.P = L.P;
-    a.vec_per_rank = per_rank_acc / 4;
-    attn_bwd_dq_convert_kernel<<<grid_cap(a.vec_per_rank * L.P), 256, 0, stream>>>(a);
-    count_launches(1);
   }
   return cuda_status(cudaGetLastError());
 }

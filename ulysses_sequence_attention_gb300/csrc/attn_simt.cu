@@ -298,8 +298,8 @@ int bwd_simt(const Layer& L, const void* const* q, const void* const* k, const v
     DK.p[r] = dk[r];
     DV.p[r] = dv[r];
   }
-  // Workspace: P fp32 dQ accumulators (unused by this path), then D.
-  float* D = reinterpret_cast<float*>(workspace) + (size_t)L.P * L.sl * L.bs * L.Hq * L.hs;
+  // Workspace: the fp32 rows D, [P][bs][Hq][sl].
+  float* D = reinterpret_cast<float*>(workspace);
   const unsigned rows = (unsigned)((L.sl + kRowsPerBlock - 1) / kRowsPerBlock);
   attn_bwd_dot_kernel<T, HS><<<dim3(rows, (unsigned)(L.bs * L.Hq), (unsigned)L.P), kWarps * 32, 0, s>>>(sh, O, DO, D);
   attn_bwd_dq_simt_kernel<T, HS><<<dim3(rows, (unsigned)(L.bs * L.Hq), (unsigned)L.P), kWarps * 32, 0, s>>>(

@@ -10,6 +10,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <type_traits>
 #include <new>
 
 #include "internal.cuh"
@@ -138,23 +139,28 @@ int ulysses_create(ulysses_t* out, int64_t sl, int64_t bs, int hc, int hkv, int 
       e = cudaMemcpy(L->d_kv_range, kv_range.data(), sizeof(int2) * kv_range.size(), cudaMemcpyHostToDevice);
     if (e == cudaSuccess)
       e = cudaMemcpy(L->d_m_order, order.data(), sizeof(int) * order.size(), cudaMemcpyHostToDevice);
-    std::vector<int2> q_range;
-    std::vector<int> n_order;
-    uly::plan_bwd_tiles(*L, q_range, n_order);
-    if (e == cudaSuccess) e = cudaMalloc(&L->d_q_range, sizeof(int2) * q_range.size());
-    if (e == cudaSuccess) e = cudaMalloc(&L->d_n_order, sizeof(int) * n_order.size());
-    if (e == cudaSuccess)
-      e = cudaMemcpy(L->d_q_range, q_range.data(), sizeof(int2) * q_range.size(), cudaMemcpyHostToDevice);
-    if (e == cudaSuccess)
-      e = cudaMemcpy(L->d_n_order, n_order.data(), sizeof(int) * n_order.size(), cudaMemcpyHostToDevice);
+    std::vector<int2> kvp, qp;
+    std::vector<int> kvo, qo;
+    uly::plan_bwd_tiles(*L, kvp, kvo, qp, qo);
+    auto upload = [&](auto** dst, const auto& v) {
+      using T = typename std::decay_t<decltype(v)>::value_type;
+      if (e == cudaSuccess) e = cudaMalloc(dst, sizeof(T) * v.size());
+      if (e == cudaSuccess) e = cudaMemcpy(*dst, v.data(), sizeof(T) * v.size(), cudaMemcpyHostToDevice);
+    };
+    upload(&L->d_kvp_range, kvp);
+    upload(&L->d_kvp_order, kvo);
+    upload(&L->d_qp_range, qp);
+    upload(&L->d_qp_order, qo);
   }
   if (e != cudaSuccess) {
     cudaFree(L->d_status);
     cudaFree(L->d_doc_offsets);
     cudaFree(L->d_kv_range);
     cudaFree(L->d_m_order);
-    cudaFree(L->d_q_range);
-    cudaFree(L->d_n_order);
+    cudaFree(L->d_kvp_range);
+    cudaFree(L->d_kvp_order);
+    cudaFree(L->d_qp_range);
+    cudaFree(L->d_qp_order);
     delete L;
     return ULYSSES_ERR_CUDA;
   }
@@ -169,17 +175,18 @@ void ulysses_destroy(ulysses_t h) {
   cudaFree(L->d_doc_offsets);
   cudaFree(L->d_kv_range);
   cudaFree(L->d_m_order);
-  cudaFree(L->d_q_range);
-  cudaFree(L->d_n_order);
+  cudaFree(L->d_kvp_range);
+  cudaFree(L->d_kvp_order);
+  cudaFree(L->d_qp_range);
+  cudaFree(L->d_qp_order);
   delete L;
 }
 
 int ulysses_workspace_size(ulysses_t h, size_t* bytes) {
   const Layer* L = reinterpret_cast<const Layer*>(h);
   if (!L || !bytes) return ULYSSES_ERR_INVALID_ARG;
-  const size_t per_rank_dq = (size_t)L->sl * L->bs * L->Hq * L->hs * sizeof(float);
-  const size_t per_rank_d = (size_t)L->bs * L->Hq * L->sl * sizeof(float);
-  *bytes = (size_t)L->P * (per_rank_dq + per_rank_d);
+  // The fp32 rows D = rowsum(dO * O): [P][bs][Hq][sl].
+  *bytes = (size_t)L->P * L->bs * L->Hq * L->sl * sizeof(float);
   return ULYSSES_OK;
 }
 

@@ -29,9 +29,13 @@ struct Layer {
   // tiles ordered by their number of key tiles (most first). Device copies.
   int2* d_kv_range = nullptr;
   int* d_m_order = nullptr;
-  // Backward: query-tile range per 128-row key tile, key tiles ordered by work.
-  int2* d_q_range = nullptr;
-  int* d_n_order = nullptr;
+  // Backward (CTA pairs): per 256-key pair tile the range of query tiles that
+  // see it, per 256-query pair tile the range of key tiles it sees; both with
+  // an order by work.
+  int2* d_kvp_range = nullptr;
+  int* d_kvp_order = nullptr;
+  int2* d_qp_range = nullptr;
+  int* d_qp_order = nullptr;
   long long timeout_cycles = 4000000000LL;  // bound of every device-side wait (~2 s)
   int inject_fault = 0;                     // test hook (ulysses_inject_fault)
   int64_t n() const { return sl / P; }          // tokens per sequence shard
@@ -83,7 +87,9 @@ void plan_tiles(const Layer& L, std::vector<int2>& kv_range, std::vector<int>& o
 int launch_attn_fwd_sm103(Layer& L, const void* const* q, const void* const* k, const void* const* v,
                           void* const* o, float* const* lse, cudaStream_t s);
 
-void plan_bwd_tiles(const Layer& L, std::vector<int2>& q_range, std::vector<int>& order);
+void plan_bwd_tiles(const Layer& L, std::vector<int2>& kv_pairs, std::vector<int>& kv_order,
+                    std::vector<int2>& q_pairs, std::vector<int>& q_order);
+size_t bwd_sm103_workspace(const Layer& L);
 int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* const* k, const void* const* v,
                           const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,
                           void* const* dk, void* const* dv, void* workspace, cudaStream_t s);
