@@ -69,9 +69,37 @@ def exchange_bytes(w, H):
 
 
 KERNEL_SOURCES = {
-    "attn_bwd_sm103_kernel": "ulysses_sequence_attention_gb300/csrc/attn_bwd_sm103.cu",
+    "attn_bwd_dkdv_kernel": "ulysses_sequence_attention_gb300/csrc/attn_bwd_sm103.cu",
+    "attn_bwd_dq_kernel": "ulysses_sequence_attention_gb300/csrc/attn_bwd_sm103.cu",
     "attn_fwd_sm103_kernel": "ulysses_sequence_attention_gb300/csrc/attn_fwd_sm103.cu",
 }
+
+
+def kernel_work(w, offs):
+    """Per timed kernel id: (CUDA kernel name, bound, algorithmic work of one step, unit).
+
+    Tensor kernels count 2*hs flops per visible (query, key) pair, head and
+    GEMM. The forward needs 2 GEMMs (S = Q K^T, O = P V). The dK/dV kernel
+    needs 4 (S, dP = dO V^T, dV = P^T dO, dK = dS^T Q), none of them repeated
+    inside it. The dQ kernel issues 3 (S, dP, dQ = dS K), of which S and dP
+    repeat the dK/dV kernel's: its algorithmic share of the 5-GEMM backward
+    is the dQ GEMM alone. Byte-bound kernels count one read and one write of
+    what they move.
+    """
+    fl2 = attn_flops(w, offs=offs) / 2.0   # one GEMM over the visible pairs
+    tok = w.sl * w.bs
+    eb = w.elem_bytes
+    return {
+        "attn_fwd": ("attn_fwd_sm103_kernel", "tensor", 2 * fl2, "flop"),
+        "bwd_dkdv": ("attn_bwd_dkdv_kernel", "tensor", 4 * fl2, "flop"),
+        "bwd_dq": ("attn_bwd_dq_kernel", "tensor", 1 * fl2, "flop"),
+        "bwd_prep": ("attn_bwd_prep_kernel", "hbm", tok * w.hc * (2 * w.hs * eb + 4), "byte"),
+        "seq_to_head": ("seq_to_head_kernel", "hbm",
+                        exchange_bytes(w, w.hc) * (2 if w.backward else 1) + 2 * exchange_bytes(w, w.hkv), "byte"),
+        "head_to_seq": ("head_to_seq_kernel", "hbm",
+                        exchange_bytes(w, w.hc) * (2 if w.backward else 1)
+                        + (2 * exchange_bytes(w, w.hkv) if w.backward else 0), "byte"),
+    }
 
 
 def captured_traffic(kernel, workload):
@@ -227,6 +255,7 @@ def run_ours(args, w, rank, world):
     barrier()
     torch.cuda.synchronize(dev)
     n0 = U.ulysses_launch_count()
+    U.ulysses_timing_enable(h, True)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -236,6 +265,12 @@ def run_ours(args, w, rank, world):
     torch.cuda.synchronize(dev)
     barrier()
     launches = U.ulysses_launch_count() - n0
+    U.ulysses_timing_enable(h, False)
+    kernels = {}
+    for i, name in enumerate(U.KERNEL_NAMES):
+        ms, n = U.ulysses_timing_read(h, i)
+        if n:
+            kernels[name] = {"total_ms": ms, "launches": n, "ms_per_step": ms / args.steps}
     clk = clocks.stop()
     elapsed_ms = t0.elapsed_time(t1)
     if U.ulysses_get_status(h) != U.ULYSSES_OK:
@@ -263,7 +298,8 @@ def run_ours(args, w, rank, world):
         e2e = run_e2e(args, w, L, x, dev, world, barrier)
 
     result = {"ms_per_step": ms_per_step, "value": value, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
-              "s2h_qkv_ms": s2h_ms, "h2s_o_ms": h2s_ms, "launches": launches, "clocks": clk, "e2e": e2e}
+              "s2h_qkv_ms": s2h_ms, "h2s_o_ms": h2s_ms, "launches": launches, "clocks": clk, "e2e": e2e,
+              "kernels": kernels}
     return result
 
 
@@ -428,17 +464,36 @@ def main():
         s2h_gbs = x_bytes / (r["s2h_qkv_ms"] * 1e-3) / 1e9
         h2s_gbs = exchange_bytes(w, w.hc) / (r["h2s_o_ms"] * 1e-3) / 1e9
         sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-        if w.backward:
-            dom = {"kernel": "attn_bwd_sm103_kernel", "achieved": bwd_tf, "ms": r["bwd_ms"], "flops": fl_bwd}
-        else:
-            dom = {"kernel": "attn_fwd_sm103_kernel", "achieved": fwd_tf, "ms": r["fwd_ms"], "flops": fl_fwd}
-        traffic, traffic_how = captured_traffic(dom["kernel"], w.name)
-        roof = {"bound": "tensor", "kernel": dom["kernel"], "achieved": dom["achieved"], "peak": sustained,
-                "unit": "TFLOP/s", "frac": dom["achieved"] / sustained, "traffic": traffic,
+        work = kernel_work(w, offs)
+        per_kernel = {}
+        for name, k in r["kernels"].items():
+            cname, bound, units, unit = work[name]
+            rate = units * args.steps / (k["total_ms"] * 1e-3)
+            per_kernel[name] = dict(k, kernel=cname, bound=bound,
+                                    **({"tflops": rate / 1e12, "frac_sustained": rate / 1e12 / sustained}
+                                       if unit == "flop" else
+                                       {"gbs": rate / 1e9, "frac_hbm": rate / 1e9 / peaks["hbm_gbs"]}))
+            if name == "bwd_dq":   # S and dP are issued again here: 3 GEMMs run, 1 is its own
+                per_kernel[name]["issued_tflops"] = 3 * rate / 1e12
+        # the dominant kernel: the largest share of the timed device time
+        top = max(r["kernels"], key=lambda n: r["kernels"][n]["total_ms"])
+        cname, bound, units, unit = work[top]
+        k = r["kernels"][top]
+        avg_ms = k["total_ms"] / k["launches"]
+        per_launch = units * args.steps / k["launches"]
+        achieved = per_launch / (avg_ms * 1e-3) / (1e12 if unit == "flop" else 1e9)
+        peak = sustained if unit == "flop" else peaks["hbm_gbs"]
+        traffic, traffic_how = captured_traffic(cname, w.name)
+        roof = {"bound": bound, "kernel": cname, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s" if unit == "flop" else "GB/s", "frac": achieved / peak, "traffic": traffic,
                 "traffic_source": traffic_how,
-                "peak_source": f"{src} bf16_tflops_sustained",
-                "frac_of_burst": dom["achieved"] / peaks["bf16_tflops"],
-                "algorithmic_tflop_per_launch": dom["flops"] / 1e12, "avg_launch_ms": dom["ms"]}
+                "peak_source": f"{src} " + ("bf16_tflops_sustained" if unit == "flop" else "hbm_gbs"),
+                "algorithmic_per_launch": per_launch, "algorithmic_unit": unit, "avg_launch_ms": avg_ms,
+                "launches": k["launches"],
+                "share_of_step": k["total_ms"] / (r["ms_per_step"] * args.steps),
+                "timing": "CUDA events recorded by the library around each launch on its stream"}
+        if unit == "flop":
+            roof["frac_of_burst"] = achieved / peaks["bf16_tflops"]
         cpu = None
         if not args.no_cpu_baseline:
             sec, val = oracle_sample(w, args.cpu_sl)
@@ -455,6 +510,7 @@ def main():
                 "cpu_baseline": cpu,
                 "e2e": r["e2e"],
                 "gpu_launches": r["launches"],
+                "kernels": per_kernel,
                 "clocks": r["clocks"],
                 "attention": {"fwd_ms": r["fwd_ms"], "fwd_tflops": fwd_tf, "fwd_frac_sustained": fwd_tf / sustained,
                               "bwd_ms": r["bwd_ms"], "bwd_tflops": bwd_tf,

@@ -229,6 +229,41 @@ int ulysses_inject_fault(ulysses_t h, int kind);
  */
 uint64_t ulysses_launch_count(void);
 
+/* The kernels of the library, as ulysses_timing_read counts them. */
+typedef enum ulysses_kernel {
+  ULYSSES_KERNEL_SEQ_TO_HEAD = 0,  /* seq->head exchange */
+  ULYSSES_KERNEL_HEAD_TO_SEQ = 1,  /* head->seq exchange, with the replica sum if P > nheads */
+  ULYSSES_KERNEL_ATTN_FWD = 2,     /* attention forward: O and LSE */
+  ULYSSES_KERNEL_BWD_PREP = 3,     /* backward, D = rowsum(dO * O) per query row */
+  ULYSSES_KERNEL_BWD_DKDV = 4,     /* backward, dK and dV */
+  ULYSSES_KERNEL_BWD_DQ = 5,       /* backward, dQ */
+  ULYSSES_KERNEL_COUNT = 6
+} ulysses_kernel;
+
+/*
+ * ulysses_timing_enable — per-kernel device time of one handle, for
+ * benchmarks. There is no counterpart in the paper.
+ *
+ * enable != 0 clears the handle's totals and starts timing. From then on,
+ * every kernel that a call of this handle enqueues is bracketed by two CUDA
+ * events recorded on the call's stream, so the time between them is that
+ * kernel's device time. enable == 0 stops timing; launches already timed
+ * stay readable. The events cost a few microseconds of host time per launch
+ * and do not change what the kernels compute. Returns ULYSSES_OK, or
+ * ULYSSES_ERR_CUDA if an event could not be created. Host only.
+ */
+int ulysses_timing_enable(ulysses_t h, int enable);
+
+/*
+ * ulysses_timing_read — device time and launch count of one kernel since the
+ * last ulysses_timing_enable(h, 1). kernel is a ulysses_kernel. This call
+ * waits for the events that the timed launches recorded (it blocks until
+ * that work has finished). total_ms and launches are host pointers; each may
+ * be NULL. Returns ULYSSES_ERR_INVALID_ARG for an unknown kernel and
+ * ULYSSES_ERR_CUDA if an event could not be recorded or read.
+ */
+int ulysses_timing_read(ulysses_t h, int kernel, double* total_ms, int64_t* launches);
+
 /*
  * ulysses_attn_bwd_noalloc — ulysses_attn_bwd for callers that cannot allocate
  * device memory. There is no counterpart in the paper: this is a deployment

@@ -107,7 +107,16 @@ def test_null_handle_calls_are_rejected(u):
     assert lib.ulysses_seq_to_head(None, 4, None, None, None) == u.ULYSSES_ERR_INVALID_ARG
     assert lib.ulysses_attn_fwd(None, None, None, None, None, None, None) == u.ULYSSES_ERR_INVALID_ARG
     assert lib.ulysses_get_status(None) == u.ULYSSES_ERR_INVALID_ARG
+    assert lib.ulysses_timing_enable(None, 1) == u.ULYSSES_ERR_INVALID_ARG
+    assert lib.ulysses_timing_read(None, 0, None, None) == u.ULYSSES_ERR_INVALID_ARG
     lib.ulysses_destroy(None)
+
+
+def test_kernel_ids_match_the_header(u):
+    text = open(HEADER).read()
+    for i, name in enumerate(u.KERNEL_NAMES):
+        assert re.search(rf"ULYSSES_KERNEL_{name.upper()}\s*=\s*{i},", text), name
+    assert re.search(rf"ULYSSES_KERNEL_COUNT\s*=\s*{u.ULYSSES_KERNEL_COUNT}\b", text)
 
 
 def declared_prototypes():

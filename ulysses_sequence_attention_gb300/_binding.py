@@ -30,6 +30,14 @@ ULYSSES_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 ULYSSES_BF16 = 0
 ULYSSES_FP32 = 1
 ULYSSES_MAX_P = 128
+ULYSSES_KERNEL_SEQ_TO_HEAD = 0
+ULYSSES_KERNEL_HEAD_TO_SEQ = 1
+ULYSSES_KERNEL_ATTN_FWD = 2
+ULYSSES_KERNEL_BWD_PREP = 3
+ULYSSES_KERNEL_BWD_DKDV = 4
+ULYSSES_KERNEL_BWD_DQ = 5
+ULYSSES_KERNEL_COUNT = 6
+KERNEL_NAMES = ("seq_to_head", "head_to_seq", "attn_fwd", "bwd_prep", "bwd_dkdv", "bwd_dq")
 
 _DTYPES = {"bf16": ULYSSES_BF16, "fp32": ULYSSES_FP32,
            torch.bfloat16: ULYSSES_BF16, torch.float32: ULYSSES_FP32}
@@ -71,6 +79,11 @@ lib.ulysses_inject_fault.argtypes = [_vp, ctypes.c_int]
 lib.ulysses_inject_fault.restype = ctypes.c_int
 lib.ulysses_launch_count.argtypes = []
 lib.ulysses_launch_count.restype = ctypes.c_uint64
+lib.ulysses_timing_enable.argtypes = [_vp, ctypes.c_int]
+lib.ulysses_timing_enable.restype = ctypes.c_int
+lib.ulysses_timing_read.argtypes = [_vp, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                    ctypes.POINTER(ctypes.c_int64)]
+lib.ulysses_timing_read.restype = ctypes.c_int
 
 
 class UlyssesError(RuntimeError):
@@ -251,3 +264,16 @@ def ulysses_set_wait_limit(h: UlyssesHandle, cycles: int):
 
 def ulysses_inject_fault(h: UlyssesHandle, kind: int):
     _check(lib.ulysses_inject_fault(h.ptr, int(kind)), "ulysses_inject_fault")
+
+
+def ulysses_timing_enable(h: UlyssesHandle, enable: bool = True):
+    """Start (clearing the totals) or stop per-kernel device timing of h."""
+    _check(lib.ulysses_timing_enable(h.ptr, 1 if enable else 0), "ulysses_timing_enable")
+
+
+def ulysses_timing_read(h: UlyssesHandle, kernel: int):
+    """(total device ms, launches) of one kernel since timing was enabled; waits for them."""
+    ms = ctypes.c_double()
+    n = ctypes.c_int64()
+    _check(lib.ulysses_timing_read(h.ptr, int(kernel), ctypes.byref(ms), ctypes.byref(n)), "ulysses_timing_read")
+    return float(ms.value), int(n.value)

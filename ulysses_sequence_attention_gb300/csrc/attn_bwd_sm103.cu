@@ -871,7 +871,9 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
     a.bs = (int)L.bs;
     a.Hq = L.Hq;
     a.rows_per_rank = (long long)L.sl * L.bs * L.Hq;
+    Timed t(L.timing, ULYSSES_KERNEL_BWD_PREP, stream);
     attn_bwd_prep_kernel<<<grid_cap(a.rows_per_rank * L.P * 16), 256, 0, stream>>>(a);
+    t.done();
     count_launches(1);
   }
   PairParams prm;
@@ -919,10 +921,12 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
       }
       const long long pairs = (long long)n_pair * nr * L.bs * (pass == 0 ? L.Hk : L.Hq);
       if (2 * pairs > 0x7fffffffLL) return ULYSSES_ERR_UNSUPPORTED;
+      Timed t(L.timing, pass == 0 ? ULYSSES_KERNEL_BWD_DKDV : ULYSSES_KERNEL_BWD_DQ, stream);
       if (pass == 0)
         attn_bwd_dkdv_kernel<<<(unsigned)(2 * pairs), kThreads, dkdv::kSmem, stream>>>(prm);
       else
         attn_bwd_dq_kernel<<<(unsigned)(2 * pairs), kThreads, dqk::kSmem, stream>>>(prm);
+      t.done();
       count_launches(1);
     }
   }

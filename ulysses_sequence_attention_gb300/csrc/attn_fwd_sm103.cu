@@ -436,7 +436,9 @@ int launch_attn_fwd_sm103(Layer& L, const void* const* q, const void* const* k, 
     }
     const long long grid = (long long)n_m * nr * L.bs * L.Hk * prm.npairs;
     if (grid > 0x7fffffffLL) return ULYSSES_ERR_UNSUPPORTED;
+    Timed t(L.timing, ULYSSES_KERNEL_ATTN_FWD, stream);
     attn_fwd_sm103_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(prm);
+    t.done();
     count_launches(1);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return ULYSSES_ERR_CUDA;

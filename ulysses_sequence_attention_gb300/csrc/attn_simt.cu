@@ -275,7 +275,9 @@ int fwd_simt(const Layer& L, const void* const* q, const void* const* k, const v
     LS.p[r] = lse[r];
   }
   dim3 grid((unsigned)((L.sl + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)(L.bs * L.Hq), (unsigned)L.P);
+  Timed t(L.timing, ULYSSES_KERNEL_ATTN_FWD, s);
   attn_fwd_simt_kernel<T, HS><<<grid, kWarps * 32, 0, s>>>(sh, Q, K, V, O, LS);
+  t.done();
   count_launches(1);
   return cuda_status(cudaGetLastError());
 }
@@ -301,11 +303,17 @@ int bwd_simt(const Layer& L, const void* const* q, const void* const* k, const v
   // Workspace: the fp32 rows D, [P][bs][Hq][sl].
   float* D = reinterpret_cast<float*>(workspace);
   const unsigned rows = (unsigned)((L.sl + kRowsPerBlock - 1) / kRowsPerBlock);
+  Timed t0(L.timing, ULYSSES_KERNEL_BWD_PREP, s);
   attn_bwd_dot_kernel<T, HS><<<dim3(rows, (unsigned)(L.bs * L.Hq), (unsigned)L.P), kWarps * 32, 0, s>>>(sh, O, DO, D);
+  t0.done();
+  Timed t1(L.timing, ULYSSES_KERNEL_BWD_DQ, s);
   attn_bwd_dq_simt_kernel<T, HS><<<dim3(rows, (unsigned)(L.bs * L.Hq), (unsigned)L.P), kWarps * 32, 0, s>>>(
       sh, Q, K, V, DO, LS, D, DQ);
+  t1.done();
+  Timed t2(L.timing, ULYSSES_KERNEL_BWD_DKDV, s);
   attn_bwd_dkdv_simt_kernel<T, HS><<<dim3(rows, (unsigned)(L.bs * L.Hk), (unsigned)L.P), kWarps * 32, 0, s>>>(
       sh, Q, K, V, DO, LS, D, DK, DV);
+  t2.done();
   count_launches(3);
   return cuda_status(cudaGetLastError());
 }

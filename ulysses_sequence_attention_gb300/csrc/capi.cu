@@ -267,6 +267,23 @@ int ulysses_inject_fault(ulysses_t h, int kind) {
 
 uint64_t ulysses_launch_count(void) { return uly::g_launches.load(std::memory_order_relaxed); }
 
+int ulysses_timing_enable(ulysses_t h, int enable) {
+  Layer* L = reinterpret_cast<Layer*>(h);
+  if (!L) return ULYSSES_ERR_INVALID_ARG;
+  if (enable) L->timing.reset();
+  L->timing.on = enable != 0;
+  return L->timing.failed ? ULYSSES_ERR_CUDA : ULYSSES_OK;
+}
+
+int ulysses_timing_read(ulysses_t h, int kernel, double* total_ms, int64_t* launches) {
+  Layer* L = reinterpret_cast<Layer*>(h);
+  if (!L || kernel < 0 || kernel >= ULYSSES_KERNEL_COUNT) return ULYSSES_ERR_INVALID_ARG;
+  L->timing.drain(L->timing.pending.size());
+  if (total_ms) *total_ms = L->timing.total_ms[kernel];
+  if (launches) *launches = L->timing.launches[kernel];
+  return L->timing.failed ? ULYSSES_ERR_CUDA : ULYSSES_OK;
+}
+
 int ulysses_get_status(ulysses_t h) {
   const Layer* L = reinterpret_cast<const Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;

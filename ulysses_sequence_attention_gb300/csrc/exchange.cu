@@ -178,7 +178,9 @@ int launch_seq_to_head(const Layer& L, int nheads, const void* const* src, void*
   a.H = H;
   a.P = L.P;
   a.replicated = replicated ? 1 : 0;
+  Timed t(L.timing, ULYSSES_KERNEL_SEQ_TO_HEAD, stream);
   seq_to_head_kernel<<<grid_for(total), kThreads, 0, stream>>>(a);
+  t.done();
   count_launches(1);
   return cuda_status(cudaGetLastError());
 }
@@ -201,6 +203,7 @@ int launch_head_to_seq(const Layer& L, int nheads, const void* const* src, void*
     }
     uint64_t g = (total + kThreads - 1) / kThreads;
     if (g > (uint64_t)kSMs * 8) g = (uint64_t)kSMs * 8;
+    Timed t(L.timing, ULYSSES_KERNEL_HEAD_TO_SEQ, stream);
     if (L.dtype == ULYSSES_BF16)
       head_to_seq_sum_kernel<__nv_bfloat16><<<(int)g, kThreads, 0, stream>>>(
           s, d, (uint32_t)total, FastDiv((uint32_t)per_shard), FastDiv((uint32_t)(H * L.hs)),
@@ -209,6 +212,7 @@ int launch_head_to_seq(const Layer& L, int nheads, const void* const* src, void*
       head_to_seq_sum_kernel<float><<<(int)g, kThreads, 0, stream>>>(
           s, d, (uint32_t)total, FastDiv((uint32_t)per_shard), FastDiv((uint32_t)(H * L.hs)),
           FastDiv((uint32_t)L.bs), FastDiv((uint32_t)L.hs), (uint32_t)n, reps);
+    t.done();
     count_launches(1);
     return cuda_status(cudaGetLastError());
   }
@@ -228,7 +232,9 @@ int launch_head_to_seq(const Layer& L, int nheads, const void* const* src, void*
   a.bs = FastDiv((uint32_t)L.bs);
   a.block_vecs = FastDiv((uint32_t)Hh * head_vecs);
   a.n = (uint32_t)n;
+  Timed t(L.timing, ULYSSES_KERNEL_HEAD_TO_SEQ, stream);
   head_to_seq_kernel<<<grid_for(total), kThreads, 0, stream>>>(a);
+  t.done();
   count_launches(1);
   return cuda_status(cudaGetLastError());
 }

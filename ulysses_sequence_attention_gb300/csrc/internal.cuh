@@ -15,6 +15,104 @@ enum : unsigned {
   STATUS_TIMEOUT = 1u,
 };
 
+// Per-kernel device time of one handle (ulysses_timing_enable / _read). Each
+// timed launch is bracketed by two events on its stream; the records wait in
+// `pending` until a read (or a full queue) synchronises them.
+struct Timing {
+  struct Rec {
+    int kernel;
+    cudaEvent_t a, b;
+  };
+  bool on = false;
+  bool failed = false;
+  std::vector<Rec> pending;
+  std::vector<cudaEvent_t> spare;
+  double total_ms[ULYSSES_KERNEL_COUNT] = {};
+  int64_t launches[ULYSSES_KERNEL_COUNT] = {};
+
+  Timing() = default;
+  Timing(const Timing&) = delete;
+  Timing& operator=(const Timing&) = delete;
+
+  cudaEvent_t take() {
+    if (!spare.empty()) {
+      cudaEvent_t e = spare.back();
+      spare.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      failed = true;
+      return nullptr;
+    }
+    return e;
+  }
+  // Called right before a launch: the start event, or null when timing is off.
+  cudaEvent_t begin(cudaStream_t s) {
+    if (!on) return nullptr;
+    cudaEvent_t a = take();
+    if (a && cudaEventRecord(a, s) != cudaSuccess) {
+      failed = true;
+      spare.push_back(a);
+      return nullptr;
+    }
+    return a;
+  }
+  // Called right after the launch with what begin returned.
+  void end(int kernel, cudaEvent_t a, cudaStream_t s) {
+    if (!a) return;
+    cudaEvent_t b = take();
+    if (!b || cudaEventRecord(b, s) != cudaSuccess) {
+      failed = true;
+      spare.push_back(a);
+      if (b) spare.push_back(b);
+      return;
+    }
+    pending.push_back({kernel, a, b});
+    if (pending.size() >= 8192) drain(4096);
+  }
+  // Folds the oldest n pending records into the totals (waits for them).
+  void drain(size_t n) {
+    n = n < pending.size() ? n : pending.size();
+    for (size_t i = 0; i < n; ++i) {
+      const Rec& r = pending[i];
+      float ms = 0.f;
+      if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess)
+        failed = true;
+      total_ms[r.kernel] += ms;
+      launches[r.kernel] += 1;
+      spare.push_back(r.a);
+      spare.push_back(r.b);
+    }
+    pending.erase(pending.begin(), pending.begin() + (long)n);
+  }
+  void reset() {
+    drain(pending.size());
+    for (int k = 0; k < ULYSSES_KERNEL_COUNT; ++k) {
+      total_ms[k] = 0.0;
+      launches[k] = 0;
+    }
+    failed = false;
+  }
+  ~Timing() {
+    for (const Rec& r : pending) {
+      cudaEventDestroy(r.a);
+      cudaEventDestroy(r.b);
+    }
+    for (cudaEvent_t e : spare) cudaEventDestroy(e);
+  }
+};
+
+// Brackets one kernel launch: `Timed t(L, ULYSSES_KERNEL_X, s); kernel<<<...>>>(...); t.done();`
+struct Timed {
+  Timing& T;
+  int kernel;
+  cudaStream_t s;
+  cudaEvent_t a;
+  Timed(Timing& T_, int k, cudaStream_t s_) : T(T_), kernel(k), s(s_), a(T_.begin(s_)) {}
+  void done() { T.end(kernel, a, s); }
+};
+
 struct Layer {
   int64_t sl = 0, bs = 0;
   int hc = 0, hkv = 0, hs = 0, P = 0, causal = 1, dtype = ULYSSES_BF16;
@@ -38,6 +136,7 @@ struct Layer {
   int* d_qp_order = nullptr;
   long long timeout_cycles = 4000000000LL;  // bound of every device-side wait (~2 s)
   int inject_fault = 0;                     // test hook (ulysses_inject_fault)
+  mutable Timing timing;                    // ulysses_timing_enable / ulysses_timing_read
   int64_t n() const { return sl / P; }          // tokens per sequence shard
   int esize() const { return dtype == ULYSSES_BF16 ? 2 : 4; }
   bool empty() const { return sl == 0 || bs == 0; }
