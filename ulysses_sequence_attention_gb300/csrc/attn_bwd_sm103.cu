@@ -131,7 +131,8 @@ enum {
   B_DP = B_S + 1,            // dP^T ready (commit, both)
   B_LOADED = B_DP + 1,       // this CTA's compute warps hold S^T, dP^T (8 warps)
   B_P = B_LOADED + 1,        // even CTA: P^T, dS^T written in both CTAs (16 warps)
-  B_DONE = B_P + 1,          // every UMMA done (commit, both)
+  B_SFREE = B_P + 1,         // even CTA: S^T copied to registers in both CTAs (16 warps)
+  B_DONE = B_SFREE + 1,      // every UMMA done (commit, both)
   B_EPI = B_DONE + 1,        // dK, dV staged (8 warps)
   B_DRAIN = B_EPI + 1,
   B_RFULL = B_DRAIN + 1,     // NR: LSE/D rows written (32 lanes, this CTA)
@@ -177,7 +178,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         cnt = crank == 0 ? 2 : 1;
       if (i >= B_RFULL && i < B_RFULL + NR) cnt = 32;
       if (i == B_LOADED || i == B_EPI || (i >= B_REMPTY && i < B_REMPTY + NR)) cnt = 8;
-      if (i == B_P) cnt = 16;
+      if (i == B_P || i == B_SFREE) cnt = 16;
       mbar_init(bar(i), cnt);
     }
     fence_mbar_init();
@@ -292,25 +293,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           umma2_commit_both(bar(B_DP));
           umma2_commit_both(bar(B_QEMPTY));
         }
-        // Per query tile i, in issue order:
-        //   S_{i+1}^T (its columns were read before P_i was signalled), then
-        //   dV += P_i^T dO_i and dK += dS_i^T Q_i interleaved, then
-        //   dP_{i+1}^T (over P_i^T and dS_i^T, after dV and dK have read them).
-        // The exponentials of tile i+1 overlap dV_i and dK_i.
-        for (int it = 0; it < n_it && ok; ++it) {
-          const int st = it % NQ;
-          const bool next = it + 1 < n_it;
-          const int st1 = (it + 1) % NQ, u1 = (it + 1) / NQ;
-          const uint32_t sq = sb + kOffStage + st * kStage;
-          if (!mbar_wait(bar(B_P), it & 1, lim)) { ok = false; break; }
-          tc_fence_after();
-          if (next) {
-            if (!mbar_wait(bar(B_QFULL + st1), u1 & 1, lim)) { ok = false; break; }
+        if (ok && n_it > 1) {
+          ok = mbar_wait(bar(B_SFREE), 0, lim) && mbar_wait(bar(B_QFULL + 1 % NQ), (1 / NQ) & 1, lim);
+          if (ok) {
             tc_fence_after();
-            issue_s(st1);
+            issue_s(1 % NQ);
             umma2_commit_both(bar(B_S));
           }
-          if (!mbar_wait(bar(B_HFULL + st), (it / NQ) & 1, lim)) { ok = false; break; }
+        }
+        // Per query tile i, in issue order:
+        //   dV += P_i^T dO_i and dK += dS_i^T Q_i, interleaved, once P_i is written;
+        //   dP_{i+1}^T, over P_i^T and dS_i^T (after dV and dK have read them);
+        //   S_{i+2}^T, over S_{i+1}^T, once the compute warps have copied that out.
+        // So S_{i+2} runs while the compute warps turn dP_{i+1} into dS_{i+1},
+        // and the exponentials of tile i+1 overlap dV_i, dK_i and dP_{i+1}.
+        for (int it = 0; it < n_it && ok; ++it) {
+          const int st = it % NQ;
+          const uint32_t sq = sb + kOffStage + st * kStage;
+          if (!mbar_wait(bar(B_P), it & 1, lim) || !mbar_wait(bar(B_HFULL + st), (it / NQ) & 1, lim)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {  // dV += P^T dO and dK += dS^T Q, interleaved
@@ -319,10 +322,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             umma2_ts(tmem + 384, tmem + 128 + kk * 8, b_mn(sq + 2 * kHalf, kk), id_tm, acc);
           }
           umma2_commit_both(bar(B_HEMPTY + st));
-          if (next) {
-            issue_dp(st1);  // overwrites P^T and dS^T only after dV and dK have read them
+          if (it + 1 < n_it) {
+            const int st1 = (it + 1) % NQ;
+            issue_dp(st1);  // its query part landed before S_{i+1} was issued
             umma2_commit_both(bar(B_DP));
-            umma2_commit_both(bar(B_QEMPTY + st1));  // the query part of tile it+1 is consumed
+            umma2_commit_both(bar(B_QEMPTY + st1));  // the query part of tile i+1 is consumed
+          }
+          if (it + 2 < n_it) {
+            const int st2 = (it + 2) % NQ;
+            if (!mbar_wait(bar(B_SFREE), (it + 1) & 1, lim) ||
+                !mbar_wait(bar(B_QFULL + st2), ((it + 2) / NQ) & 1, lim)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(st2);
+            umma2_commit_both(bar(B_S));
           }
         }
         if (ok)
@@ -378,6 +393,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + lane_base + 0 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pf[0]));
       tmem_ld32(tmem + lane_base + 32 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pf[32]));
       tmem_ld_wait();
+      tc_fence_before();
+      warp_arrive_leader(bar(B_SFREE), crank);  // S^T may be overwritten by S of tile it+2
       const float* rs = rows + rsl * 256;
       const int i0 = m * 128 + 64 * h;
       const bool full = qlo <= i0 && i0 + 63 <= qhi;
