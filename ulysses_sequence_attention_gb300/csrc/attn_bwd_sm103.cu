@@ -214,8 +214,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int m = qr.x + it % nm;
         const uint32_t sq = sb + kOffStage + st * kStage;
         const int q0 = m * 128;
-        // LSE (log2 units) and D rows of the tile; rows past the end get
-        // LSE = +inf, so that P = 0 there.
+        // -LSE (log2 units) and D rows of the tile; rows past the end get
+        // -LSE = -inf, so that P = 0 there.
         const int rsl = it % NR;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(B_REMPTY + rsl), ((it / NR) & 1) ^ 1, lim));
         if (!ok) break;
@@ -225,7 +225,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 4; ++e) {
           const int i = q0 + lane * 4 + e;
           const bool in = i < p.sl;
-          rs[lane * 4 + e] = in ? p.lse[rl][base + i] * 1.4426950408889634f : INFINITY;
+          rs[lane * 4 + e] = in ? -(p.lse[rl][base + i] * 1.4426950408889634f) : -INFINITY;
           rs[128 + lane * 4 + e] = in ? p.D[rl][base + i] : 0.f;
         }
         mbar_arrive(bar(B_RFULL + rsl));
@@ -398,15 +398,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const float* rs = rows + rsl * 256;
       const int i0 = m * 128 + 64 * h;
       const bool full = qlo <= i0 && i0 + 63 <= qhi;
+      // P^T = 2^(S^T * scale*log2(e) - LSE), two query columns per packed op
+      const uint64_t sc2 = f2(sl2, sl2);
+      const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(rs + 64 * h);
+      uint64_t pp[32];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float pv = ex2_approx(fmaf(__uint_as_float(pf[c]), sl2, -rs[64 * h + c]));
-        if (!full) {
-          const int i = i0 + c;
-          if (i < qlo || i > qhi) pv = 0.f;
+      for (int c = 0; c < 32; ++c) pp[c] = f2_ex2(f2_fma(f2_bits(pf[2 * c], pf[2 * c + 1]), sc2, nl2[c]));
+      if (!full) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          float p0, p1;
+          f2_split(pp[c], p0, p1);
+          const int i = i0 + 2 * c;
+          if (i < qlo || i > qhi) p0 = 0.f;
+          if (i + 1 < qlo || i + 1 > qhi) p1 = 0.f;
+          pp[c] = f2(p0, p1);
         }
-        pf[c] = __float_as_uint(pv);
       }
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) pk[c] = f2_pack_bf16(pp[c]);
       ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DP), it & 1, lim));
       if (!ok) break;
       tc_fence_after();
@@ -416,15 +427,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       warp_arrive_local(bar(B_LOADED));  // both halves read before either is overwritten
-      uint32_t pk[32], dk[32];
+      // dS^T = P^T * (dP^T - D)
+      const uint64_t* d2 = reinterpret_cast<const uint64_t*>(rs + 128 + 64 * h);
+      uint32_t dk[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float p0 = __uint_as_float(pf[2 * c]), p1 = __uint_as_float(pf[2 * c + 1]);
-        const float d0 = p0 * (__uint_as_float(dp[2 * c]) - rs[128 + 64 * h + 2 * c]);
-        const float d1 = p1 * (__uint_as_float(dp[2 * c + 1]) - rs[128 + 64 * h + 2 * c + 1]);
-        pk[c] = pack_bf16x2(p0, p1);
-        dk[c] = pack_bf16x2(d0, d1);
-      }
+      for (int c = 0; c < 32; ++c) dk[c] = f2_pack_bf16(f2_mul(pp[c], f2_sub(f2_bits(dp[2 * c], dp[2 * c + 1]), d2[c])));
       warp_arrive_local(bar(B_REMPTY + rsl));  // done with this tile's LSE/D rows
       ok = __all_sync(0xffffffffu, mbar_wait(bar(B_LOADED), it & 1, lim));
       if (!ok) break;
@@ -686,7 +693,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       Di = p.D[rl][base];
     }
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const float sl2 = p.scale_log2;
+    const uint64_t sc2 = f2(p.scale_log2, p.scale_log2), nl2 = f2(-lse2, -lse2), D2 = f2(Di, Di);
     bool ok = true;
     for (int jj = 0; jj < n_kv; ++jj) {
       const int k0 = (kr.x + jj) * 128 + 64 * h;
@@ -699,14 +706,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + lane_base + scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&pf[32]));
       tmem_ld_wait();
       const bool full = klo <= k0 && k0 + 63 <= khi;
+      uint64_t pp[32];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float pv = ex2_approx(fmaf(__uint_as_float(pf[c]), sl2, -lse2));
-        if (!full) {
-          const int key = k0 + c;
-          if (key < klo || key > khi) pv = 0.f;
+      for (int c = 0; c < 32; ++c) pp[c] = f2_ex2(f2_fma(f2_bits(pf[2 * c], pf[2 * c + 1]), sc2, nl2));
+      if (!full) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          float p0, p1;
+          f2_split(pp[c], p0, p1);
+          const int key = k0 + 2 * c;
+          if (key < klo || key > khi) p0 = 0.f;
+          if (key + 1 < klo || key + 1 > khi) p1 = 0.f;
+          pp[c] = f2(p0, p1);
         }
-        pf[c] = __float_as_uint(pv);
       }
       ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DP), jj & 1, lim));
       if (!ok) break;
@@ -719,11 +731,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       warp_arrive_local(bar(B_LOADED));
       uint32_t dk[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float d0 = __uint_as_float(pf[2 * c]) * (__uint_as_float(dp[2 * c]) - Di);
-        const float d1 = __uint_as_float(pf[2 * c + 1]) * (__uint_as_float(dp[2 * c + 1]) - Di);
-        dk[c] = pack_bf16x2(d0, d1);
-      }
+      for (int c = 0; c < 32; ++c) dk[c] = f2_pack_bf16(f2_mul(pp[c], f2_sub(f2_bits(dp[2 * c], dp[2 * c + 1]), D2)));
       ok = __all_sync(0xffffffffu, mbar_wait(bar(B_LOADED), jj & 1, lim));
       if (!ok) break;
       tc_fence_after();

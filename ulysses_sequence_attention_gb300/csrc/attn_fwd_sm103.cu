@@ -294,22 +294,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103_kernel(const __gri
             uint32_t o[32];
             tmem_ld32(t_o + 32 * q, o);
             tmem_ld_wait();
+            const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+            for (int c = 0; c < 16; ++c) {
+              const uint64_t v = f2_mul(f2_bits(o[2 * c], o[2 * c + 1]), a2);
+              float lo, hi;
+              f2_split(v, lo, hi);
+              o[2 * c] = __float_as_uint(lo);
+              o[2 * c + 1] = __float_as_uint(hi);
+            }
             tmem_st32(t_o + 32 * q, o);
           }
           tmem_st_wait();
         }
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-        float sum = 0.f;
+        // P = 2^(S * scale*log2(e) - m), two keys per packed op; four partial row sums
+        const uint64_t sc2 = f2(sl2, sl2), nm2 = f2(-msub, -msub);
+        uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * c]), sl2, -msub));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -msub));
-          sum += p0 + p1;
-          s[c] = pack_bf16x2(p0, p1);
+          const uint64_t pp = f2_ex2(f2_fma(f2_bits(s[2 * c], s[2 * c + 1]), sc2, nm2));
+          sum2[c & 3] = f2_add(sum2[c & 3], pp);
+          s[c] = f2_pack_bf16(pp);
         }
-        l += sum;
+        float s0, s1;
+        f2_split(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), s0, s1);
+        l += s0 + s1;
         tmem_st32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
         tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
         tmem_st_wait();
@@ -322,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103_kernel(const __gri
         // Normalise O and stage it, 128-byte swizzled, in this tile's Q buffer
         // (free: every UMMA has completed), then one TMA store per half.
         const float inv = 1.f / l;
+        const uint64_t inv2 = f2(inv, inv);
         const uint32_t stage = sQ0 + t * kTile;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -333,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103_kernel(const __gri
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              w[e] = pack_bf16x2(__uint_as_float(o[c4 * 8 + 2 * e]) * inv, __uint_as_float(o[c4 * 8 + 2 * e + 1]) * inv);
+              w[e] = f2_pack_bf16(f2_mul(f2_bits(o[c4 * 8 + 2 * e], o[c4 * 8 + 2 * e + 1]), inv2));
             const int chunk = q * 4 + c4;  // 16-byte chunk of the 256-byte row
             const uint32_t addr = stage + (chunk >> 3) * (kTile / 2) + sw128_offset(rq, chunk & 7);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),

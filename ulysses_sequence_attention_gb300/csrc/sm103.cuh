@@ -293,6 +293,57 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Packed fp32 pairs: the .f32x2 forms of add, sub, mul and fma do the work of
+// two fp32 instructions in one, with the same rounding (.rn) per lane. On this
+// SM, scalar fp32 add/fma instructions from the softmax warps slow the tensor
+// pipe's UMMAs (measured: 64 -> 87 cycles per M=256 UMMA under dense scalar
+// FMA; unchanged under the packed forms), so the per-element softmax
+// arithmetic is written with these. A pair is a 64-bit value, low lane first.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_bits(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// 2^x of both lanes (two MUFU operations) and the bf16x2 pack of the result.
+__device__ __forceinline__ uint64_t f2_ex2(uint64_t x) {
+  float lo, hi;
+  f2_split(x, lo, hi);
+  return f2(ex2_approx(lo), ex2_approx(hi));
+}
+__device__ __forceinline__ uint32_t f2_pack_bf16(uint64_t v) {
+  float lo, hi;
+  f2_split(v, lo, hi);
+  return pack_bf16x2(lo, hi);
+}
+
 // Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` inside a
 // 128-byte-swizzled region whose rows are 128 bytes apart and whose base is
 // 1024-byte aligned: the chunk index is XORed with the row index mod 8.
