@@ -80,21 +80,6 @@ struct PairParams {
 
 __device__ __forceinline__ void pair_status(const PairParams& p) { atomicOr(p.status, STATUS_TIMEOUT); }
 
-// Per-warp arrival on a barrier of the even CTA (remote from the odd one).
-__device__ __forceinline__ void warp_arrive_leader(uint32_t bar_local, uint32_t crank) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) {
-    if (crank == 0)
-      mbar_arrive(bar_local);
-    else
-      mbar_arrive_cluster(mapa(bar_local, 0));
-  }
-}
-__device__ __forceinline__ void warp_arrive_local(uint32_t bar_local) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar_local);
-}
-
 // Stage a thread's row of a 128-row x 64-column bf16 block (64 values as 32
 // packed words), 128-byte swizzled, at `region`.
 __device__ __forceinline__ void stage_row64(uint32_t region, int row, const uint32_t (&w)[32]) {
@@ -829,10 +814,11 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constan
 }  // namespace
 
 // Pair schedules. dK/dV: per 256-key pair tile, the range of 128-row query
-// tiles that can see any of its keys. dQ: per 256-query pair tile, the range
-// of 128-row key tiles any of its queries can see. Both ordered by work.
-void plan_bwd_tiles(const Layer& L, std::vector<int2>& kv_pairs, std::vector<int>& kv_order,
-                    std::vector<int2>& q_pairs, std::vector<int>& q_order) {
+// tiles that can see any of its keys. Forward and dQ: per 256-query pair
+// tile, the range of 128-key tiles any of its queries can see. Both ordered
+// by work, most first.
+void plan_pair_tiles(const Layer& L, std::vector<int2>& kv_pairs, std::vector<int>& kv_order,
+                     std::vector<int2>& q_pairs, std::vector<int>& q_order) {
   const int sl = (int)L.sl;
   const int n_pair = (sl + 255) / 256;
   auto doc = [&](int t) {

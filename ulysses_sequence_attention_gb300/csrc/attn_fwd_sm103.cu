@@ -8,27 +8,35 @@
 // causal, and no key visible across a document boundary.
 //
 // Design (bf16 in, fp32 accumulate, head size 128):
-//  * One CTA = two 128-row query tiles of two query heads of the same GQA
-//    group, at the same rows. Both tiles see the same key range and the same
-//    mask, and every K/V tile that TMA brings into shared memory feeds both.
+//  * A cluster of two CTAs runs M=256 UMMAs (tcgen05 .cta_group::2): the
+//    even CTA owns query rows [256m, 256m+128), the odd one the next 128.
+//    Each CTA holds two query tiles, of two query heads of the same GQA
+//    group at the same rows: every K/V tile in shared memory feeds both.
+//  * Per 128-key tile each CTA loads half of K (its 64 keys x 128, the N
+//    half of the B operand of S = Q K^T) and half of V (128 keys x its 64
+//    head columns, the N half of the B operand of O += P V). The even CTA's
+//    UMMA issuer drives both CTAs' tensor cores; the odd CTA forwards its
+//    load completions to the even CTA's barriers.
 //  * Warp roles: warps 0-3 and 4-7 are the softmax warpgroups of tile 0 and
 //    tile 1 (one query row per thread, which is one TMEM lane); warp 8 issues
-//    the TMA loads; warp 9 allocates tensor memory and issues the UMMAs;
-//    warps 10-11 only complete the third warpgroup. The block launches with
-//    168 registers per thread; the third warpgroup gives up 112 of them
-//    (down to 56) and the softmax warpgroups take them (up to 224):
-//    2*128*224 + 128*56 = 384*168.
+//    the TMA loads; warp 9 allocates tensor memory (both CTAs) and, in the
+//    even CTA, issues the UMMAs; warp 10 of the odd CTA forwards. The block
+//    launches with 168 registers per thread; the third warpgroup gives up
+//    112 of them (down to 56) and the softmax warpgroups take them (up to
+//    224): 2*128*224 + 128*56 = 384*168.
 //  * Tensor memory (512 columns): S of tile t at columns [128t, 128t+128),
 //    overwritten in place by P (bf16, 64 columns); O of tile t at
 //    [256+128t, 384+128t). P feeds O += P V straight from tensor memory.
 //  * The two tiles ping-pong: while one warpgroup exponentiates its S, the
-//    tensor core runs the other tile's P V and Q K^T.
+//    tensor cores run the other tile's P V and Q K^T.
 //  * Online softmax in the log2 domain. O is rescaled only when a row's max
 //    grows by more than 8 (a factor 256), so the rescale is rare. The final
-//    O = sum p v / sum p is exact whatever max was used.
-//  * Key tiles outside the visible range are never loaded (causal and
-//    per-document block skipping). The host orders the query tiles by their
-//    number of key tiles, most first, so the longest CTAs start first.
+//    O = sum p v / sum p is exact whatever max was used. The per-element
+//    arithmetic uses packed fp32 pairs, which leave the tensor pipe's rate
+//    alone.
+//  * Key tiles outside the visible range of the 256 rows are never loaded
+//    (causal and per-document block skipping). The host orders the row
+//    blocks by their number of key tiles, most first.
 //  * Every mbarrier wait is bounded. A wait that runs out sets the handle's
 //    status word, and the kernel winds down without touching more data.
 #include <math.h>
@@ -53,22 +61,23 @@ constexpr int kRegsLaunch = (65536 / kThreads) / 8 * 8;  // registers per thread
 static_assert(kRegsSoftmax >= kRegsLaunch && kRegsOther <= kRegsLaunch, "register split directions");
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsOther <= kThreads * kRegsLaunch,
               "register split must add up to the launch budget");
-constexpr int NS = 2;                            // K/V pipeline stages
-constexpr uint32_t kTile = 128 * 128 * 2;        // one 128x128 bf16 tile
-constexpr uint32_t kOffQ = 0;                    // 2 tiles
-constexpr uint32_t kOffK = 2 * kTile;            // NS tiles
-constexpr uint32_t kOffV = kOffK + NS * kTile;   // NS tiles
-constexpr uint32_t kOffBar = kOffV + NS * kTile;
-constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;  // + barriers + alignment slack
+constexpr int NS = 4;                              // K/V pipeline stages
+constexpr uint32_t kTile = 128 * 128 * 2;          // one 128x128 bf16 tile: 32 KB
+constexpr uint32_t kHalf = kTile / 2;              // 16 KB
+constexpr uint32_t kOffQ = 0;                      // 2 query tiles
+constexpr uint32_t kOffStage = 2 * kTile;          // NS stages: K half (16 KB), then V half (16 KB)
+constexpr uint32_t kStage = 2 * kHalf;
+constexpr uint32_t kOffBar = kOffStage + NS * kStage;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
 
 struct FwdParams {
-  CUtensorMap tq[kRanksPerLaunch];
-  CUtensorMap tk[kRanksPerLaunch];
-  CUtensorMap tv[kRanksPerLaunch];
-  CUtensorMap to[kRanksPerLaunch];
+  CUtensorMap tq[kRanksPerLaunch];   // Q, boxes of 64 columns x 128 rows
+  CUtensorMap tk[kRanksPerLaunch];   // K, boxes of 64 columns x 64 rows
+  CUtensorMap tv[kRanksPerLaunch];   // V, boxes of 64 columns x 128 rows
+  CUtensorMap to[kRanksPerLaunch];   // O (store), boxes of 64 columns x 128 rows
   float* lse[kRanksPerLaunch];
-  const int2* kv_range;   // per query tile: first and last key tile (inclusive)
-  const int* m_order;     // query tiles, most key tiles first
+  const int2* kv_range;   // per 256-row block: first and last key tile (inclusive)
+  const int* m_order;     // row blocks, most key tiles first
   const int32_t* doc_offsets;
   unsigned* status;
   long long timeout;      // clock cycles per wait
@@ -79,59 +88,64 @@ struct FwdParams {
 
 // Barrier indices.
 enum {
-  B_QFULL = 0,
-  B_KFULL = 1,             // NS
-  B_VFULL = B_KFULL + NS,  // NS
-  B_KEMPTY = B_VFULL + NS, // NS
-  B_VEMPTY = B_KEMPTY + NS,// NS
-  B_SFULL = B_VEMPTY + NS, // 2
-  B_PFULL = B_SFULL + 2,   // 2
-  B_OFINAL = B_PFULL + 2,  // 2
-  B_OSTAGE = B_OFINAL + 2, // 2
+  B_QFULL = 0,               // Q landed (even CTA: + the odd CTA's forward)
+  B_KVFULL = 1,              // NS: K/V halves landed (even CTA: + forward)
+  B_KVEMPTY = B_KVFULL + NS, // NS: stage consumed (commit, both CTAs)
+  B_SFULL = B_KVEMPTY + NS,  // 2: S of tile t ready (commit, both)
+  B_PFULL = B_SFULL + 2,     // 2: even CTA: P of tile t written in both CTAs (8 warps)
+  B_OFINAL = B_PFULL + 2,    // 2: every UMMA of tile t done (commit, both)
+  B_OSTAGE = B_OFINAL + 2,   // 2: O of tile t staged (128 threads)
   B_DRAIN = B_OSTAGE + 2,
   B_COUNT
 };
+static_assert(8 * B_COUNT + 4 <= 256, "barrier area");
 
-__global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    attn_fwd_sm103_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 256);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * B_COUNT);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   const uint32_t sQ0 = sb + kOffQ;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_rank();
 
-  // Work item: (query tile, rank, batch, kv head, pair of query heads).
+  // Pair work item: (256-row block, rank, batch, kv head, pair of query heads).
+  const int pair = blockIdx.x >> 1;
   const int units = p.nranks * p.bs * p.Hk * p.npairs;
-  const int m = p.m_order[blockIdx.x / units];
-  int rest = blockIdx.x % units;
-  const int pair = rest % p.npairs;
+  const int mp = p.m_order[pair / units];
+  int rest = pair % units;
+  const int hpair = rest % p.npairs;
   rest /= p.npairs;
   const int hk = rest % p.Hk;
   rest /= p.Hk;
   const int b = rest % p.bs;
   const int rl = rest / p.bs;
-  const int hq0 = hk * p.group + 2 * pair;
-  const int ntile = (2 * pair + 1 < p.group) ? 2 : 1;
-  const int2 kr = p.kv_range[m];
+  const int hq0 = hk * p.group + 2 * hpair;
+  const int ntile = (2 * hpair + 1 < p.group) ? 2 : 1;
+  const int2 kr = p.kv_range[mp];
   const int n_kv = kr.y - kr.x + 1;
+  const int q0 = mp * 256 + 128 * (int)crank;  // this CTA's first query row
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
-      if (i == B_PFULL || i == B_PFULL + 1 || i == B_OSTAGE || i == B_OSTAGE + 1) cnt = 128;
+      if (i == B_QFULL || (i >= B_KVFULL && i < B_KVFULL + NS)) cnt = crank == 0 ? 2 : 1;
+      if (i == B_PFULL || i == B_PFULL + 1) cnt = 8;
+      if (i == B_OSTAGE || i == B_OSTAGE + 1) cnt = 128;
       mbar_init(bar(i), cnt);
     }
     fence_mbar_init();
   }
   if (warp == 9) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
+    tmem_alloc2(smem_u32(tmem_slot), 512);
+    tmem_relinquish2();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // barriers of both CTAs exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const long long lim = p.timeout;
@@ -139,103 +153,106 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103_kernel(const __gri
   if (warp >= 8) {
     regs_dec<kRegsOther>();
     if (warp == 8) {
-    // ----------------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      bool ok = true;
-      int last_k[NS], last_v[NS];  // last phase armed on each full barrier (-1: none)
-      for (int i = 0; i < NS; ++i) last_k[i] = last_v[i] = -1;
-      mbar_expect_tx(bar(B_QFULL), ntile * kTile);
-      for (int t = 0; t < ntile; ++t) {
-        const uint32_t dst = sQ0 + t * kTile;
-        tma_load_4d(dst, &p.tq[rl], bar(B_QFULL), 0, hq0 + t, b, m * 128);
-        tma_load_4d(dst + kTile / 2, &p.tq[rl], bar(B_QFULL), 64, hq0 + t, b, m * 128);
-      }
-      for (int jj = 0; jj < (p.skip_kv_loads ? 0 : n_kv); ++jj) {
-        const int st = jj % NS, u = jj / NS;
-        const int row = (kr.x + jj) * 128;
-        if (!mbar_wait(bar(B_KEMPTY + st), (u & 1) ^ 1, lim)) { ok = false; break; }
-        mbar_expect_tx(bar(B_KFULL + st), kTile);
-        const uint32_t dk = sb + kOffK + st * kTile;
-        tma_load_4d(dk, &p.tk[rl], bar(B_KFULL + st), 0, hk, b, row);
-        tma_load_4d(dk + kTile / 2, &p.tk[rl], bar(B_KFULL + st), 64, hk, b, row);
-        last_k[st] = u;
-        if (!mbar_wait(bar(B_VEMPTY + st), (u & 1) ^ 1, lim)) { ok = false; break; }
-        mbar_expect_tx(bar(B_VFULL + st), kTile);
-        const uint32_t dv = sb + kOffV + st * kTile;
-        tma_load_4d(dv, &p.tv[rl], bar(B_VFULL + st), 0, hk, b, row);
-        tma_load_4d(dv + kTile / 2, &p.tv[rl], bar(B_VFULL + st), 64, hk, b, row);
-        last_v[st] = u;
-      }
-      if (!ok) atomicOr(p.status, STATUS_TIMEOUT);
-      // Let every copy this thread started land before the CTA can exit.
-      mbar_wait(bar(B_QFULL), 0, lim);
-      for (int i = 0; i < NS; ++i) {
-        if (last_k[i] >= 0) mbar_wait(bar(B_KFULL + i), last_k[i] & 1, lim);
-        if (last_v[i] >= 0) mbar_wait(bar(B_VFULL + i), last_v[i] & 1, lim);
-      }
-    }
-    __syncwarp();
-    } else if (warp == 9) {
-    // ----------------------------------------------------------------- UMMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // Q (K-major) x K (K-major)
-      constexpr uint32_t idesc_o = idesc_bf16_f32(128, 128, 0, 1);  // P (tmem) x V (MN-major)
-      auto issue_s = [&](int t, int st) {
-        const uint32_t q = sQ0 + t * kTile, k = sb + kOffK + st * kTile;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTile / 2) + (kk & 3) * 32;
-          umma_ss(tmem + t * 128, sdesc_sw128(q + off, 0, 1024), sdesc_sw128(k + off, 0, 1024), idesc_s, kk > 0);
-        }
-      };
-      auto issue_pv = [&](int t, int st, bool acc) {
-        const uint32_t v = sb + kOffV + st * kTile;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, sdesc_sw128(v + kk * 2048, kTile / 2, 1024), idesc_o,
-                  (acc || kk > 0) ? 1u : 0u);
-      };
-      bool ok = mbar_wait(bar(B_QFULL), 0, lim) && mbar_wait(bar(B_KFULL), 0, lim);
-      if (ok) {
-        tc_fence_after();
+      // ----------------------------------------------------------------- TMA producer
+      if (lane == 0) {
+        bool ok = true;
+        int last[NS];  // last phase armed on each full barrier (-1: none)
+        for (int i = 0; i < NS; ++i) last[i] = -1;
+        mbar_expect_tx(bar(B_QFULL), ntile * kTile);
         for (int t = 0; t < ntile; ++t) {
-          issue_s(t, 0);
-          umma_commit(bar(B_SFULL + t));
+          const uint32_t dst = sQ0 + t * kTile;
+          tma_load_4d(dst, &p.tq[rl], bar(B_QFULL), 0, hq0 + t, b, q0);
+          tma_load_4d(dst + kHalf, &p.tq[rl], bar(B_QFULL), 64, hq0 + t, b, q0);
         }
-        umma_commit(bar(B_KEMPTY));
+        for (int jj = 0; jj < (p.skip_kv_loads ? 0 : n_kv); ++jj) {
+          const int st = jj % NS, u = jj / NS;
+          const int k0 = (kr.x + jj) * 128;
+          if (!mbar_wait(bar(B_KVEMPTY + st), (u & 1) ^ 1, lim)) { ok = false; break; }
+          const uint32_t sk = sb + kOffStage + st * kStage;
+          mbar_expect_tx(bar(B_KVFULL + st), kStage);
+          // K rows [k0 + 64c, +64) (the N half of B for S = Q K^T), K-major in two 64-column boxes
+          tma_load_4d(sk, &p.tk[rl], bar(B_KVFULL + st), 0, hk, b, k0 + 64 * (int)crank);
+          tma_load_4d(sk + kHalf / 2, &p.tk[rl], bar(B_KVFULL + st), 64, hk, b, k0 + 64 * (int)crank);
+          // V columns [64c, 64c+64) of all 128 key rows (the N half of B for O += P V), MN-major
+          tma_load_4d(sk + kHalf, &p.tv[rl], bar(B_KVFULL + st), 64 * (int)crank, hk, b, k0);
+          last[st] = u;
+        }
+        if (!ok) atomicOr(p.status, STATUS_TIMEOUT);
+        // Let every copy this thread started land before the CTA can exit.
+        mbar_wait(bar(B_QFULL), 0, lim);
+        for (int i = 0; i < NS; ++i)
+          if (last[i] >= 0) mbar_wait(bar(B_KVFULL + i), last[i] & 1, lim);
       }
-      for (int jj = 0; jj < n_kv && ok; ++jj) {
-        const int st = jj % NS, u = jj / NS;
-        const bool next = jj + 1 < n_kv;
-        const int st1 = (jj + 1) % NS, u1 = (jj + 1) / NS;
-        if (!mbar_wait(bar(B_VFULL + st), u & 1, lim)) { ok = false; break; }
-        for (int t = 0; t < ntile && ok; ++t) {
-          if (!mbar_wait(bar(B_PFULL + t), jj & 1, lim)) { ok = false; break; }
+      __syncwarp();
+    } else if (warp == 9 && crank == 0) {
+      // ----------------------------------------------------------------- UMMA issuer (even CTA)
+      if (lane == 0) {
+        constexpr uint32_t idesc_s = idesc_bf16_f32(256, 128, 0, 0);  // Q (K-major) x K (K-major)
+        constexpr uint32_t idesc_o = idesc_bf16_f32(256, 128, 0, 1);  // P (tmem) x V (MN-major)
+        auto issue_s = [&](int t, int st) {
+          const uint32_t q = sQ0 + t * kTile, k = sb + kOffStage + st * kStage;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma2_ss(tmem + t * 128, sdesc_sw128(q + (kk >> 2) * kHalf + (kk & 3) * 32, 0, 1024),
+                     sdesc_sw128(k + (kk >> 2) * (kHalf / 2) + (kk & 3) * 32, 0, 1024), idesc_s, kk > 0);
+        };
+        auto issue_pv = [&](int t, int st, bool acc) {
+          const uint32_t v = sb + kOffStage + st * kStage + kHalf;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma2_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, sdesc_sw128(v + kk * 2048, kHalf, 1024), idesc_o,
+                     (acc || kk > 0) ? 1u : 0u);
+        };
+        bool ok = mbar_wait(bar(B_QFULL), 0, lim) && mbar_wait(bar(B_KVFULL), 0, lim);
+        if (ok) {
           tc_fence_after();
-          issue_pv(t, st, jj > 0);
-          if (next) {
-            if (t == 0) {
-              if (!mbar_wait(bar(B_KFULL + st1), u1 & 1, lim)) { ok = false; break; }
-              tc_fence_after();
-            }
-            issue_s(t, st1);
-            umma_commit(bar(B_SFULL + t));
+          for (int t = 0; t < ntile; ++t) {
+            issue_s(t, 0);
+            umma2_commit_both(bar(B_SFULL + t));
           }
         }
-        if (!ok) break;
-        umma_commit(bar(B_VEMPTY + st));
-        if (next) umma_commit(bar(B_KEMPTY + st1));
+        for (int jj = 0; jj < n_kv && ok; ++jj) {
+          const int st = jj % NS;
+          const bool next = jj + 1 < n_kv;
+          const int st1 = (jj + 1) % NS, u1 = (jj + 1) / NS;
+          if (next && !mbar_wait(bar(B_KVFULL + st1), u1 & 1, lim)) { ok = false; break; }
+          for (int t = 0; t < ntile; ++t) {
+            if (!mbar_wait(bar(B_PFULL + t), jj & 1, lim)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(t, st, jj > 0);
+            if (next) {
+              issue_s(t, st1);  // over P of this tile: after the P V above has read it
+              umma2_commit_both(bar(B_SFULL + t));
+            }
+          }
+          if (!ok) break;
+          umma2_commit_both(bar(B_KVEMPTY + st));
+        }
+        if (ok) {
+          for (int t = 0; t < ntile; ++t) umma2_commit_both(bar(B_OFINAL + t));
+        } else {
+          atomicOr(p.status, STATUS_TIMEOUT);
+        }
+        // Every UMMA issued so far completes before the tensor memory is freed.
+        umma2_commit_both(bar(B_DRAIN));
+        mbar_wait(bar(B_DRAIN), 0, lim);
       }
-      if (ok) {
-        for (int t = 0; t < ntile; ++t) umma_commit(bar(B_OFINAL + t));
-      } else {
-        atomicOr(p.status, STATUS_TIMEOUT);
+      __syncwarp();
+    } else if (warp == 10 && crank == 1) {
+      // ----------------------------------------------------------------- forwarder (odd CTA)
+      // The even CTA's UMMAs read this CTA's shared memory: tell it when the
+      // loads have landed.
+      if (lane == 0) {
+        bool ok = mbar_wait(bar(B_QFULL), 0, lim);
+        if (ok) mbar_arrive_cluster(mapa(bar(B_QFULL), 0));
+        for (int jj = 0; jj < (p.skip_kv_loads ? 0 : n_kv) && ok; ++jj) {
+          const int st = jj % NS, u = jj / NS;
+          ok = mbar_wait(bar(B_KVFULL + st), u & 1, lim);
+          if (ok) mbar_arrive_cluster(mapa(bar(B_KVFULL + st), 0));
+        }
+        if (!ok) atomicOr(p.status, STATUS_TIMEOUT);
       }
-      // Every UMMA issued so far completes before the tensor memory is freed.
-      umma_commit(bar(B_DRAIN));
-      mbar_wait(bar(B_DRAIN), 0, lim);
-    }
-    __syncwarp();
+      __syncwarp();
     }
   } else {
     regs_inc<kRegsSoftmax>();
@@ -243,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103_kernel(const __gri
     const int t = warp >> 2;
     if (t < ntile) {
       const int rq = (warp & 3) * 32 + lane;  // row within the tile = TMEM lane
-      const int row = m * 128 + rq;
+      const int row = q0 + rq;
       const int hq = hq0 + t;
       int lo = 0, hi = -1;                      // visible keys [lo, hi] of this row
       if (row < p.sl) {
@@ -255,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103_kernel(const __gri
       const uint32_t t_s = tmem + lane_base + t * 128;
       const uint32_t t_o = tmem + lane_base + 256 + t * 128;
       const float sl2 = p.scale_log2;
+      const uint64_t sc2 = f2(sl2, sl2);
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;
       for (int jj = 0; jj < n_kv; ++jj) {
@@ -289,19 +307,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103_kernel(const __gri
         if (jj > 0 && __any_sync(0xffffffffu, need)) {
           // O holds the sum over earlier key tiles (their P V completed before
           // this tile's S was committed); scale it to the new max.
+          const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint32_t o[32];
             tmem_ld32(t_o + 32 * q, o);
             tmem_ld_wait();
-            const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-              const uint64_t v = f2_mul(f2_bits(o[2 * c], o[2 * c + 1]), a2);
-              float lo, hi;
-              f2_split(v, lo, hi);
-              o[2 * c] = __float_as_uint(lo);
-              o[2 * c + 1] = __float_as_uint(hi);
+              float lo2, hi2;
+              f2_split(f2_mul(f2_bits(o[2 * c], o[2 * c + 1]), a2), lo2, hi2);
+              o[2 * c] = __float_as_uint(lo2);
+              o[2 * c + 1] = __float_as_uint(hi2);
             }
             tmem_st32(t_o + 32 * q, o);
           }
@@ -309,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103_kernel(const __gri
         }
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
         // P = 2^(S * scale*log2(e) - m), two keys per packed op; four partial row sums
-        const uint64_t sc2 = f2(sl2, sl2), nm2 = f2(-msub, -msub);
+        const uint64_t nm2 = f2(-msub, -msub);
         uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
@@ -324,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103_kernel(const __gri
         tmem_st32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(B_PFULL + t));
+        warp_arrive_leader(bar(B_PFULL + t), crank);
       }
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_OFINAL + t), 0, lim));
       if (ok) {
@@ -346,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103_kernel(const __gri
             for (int e = 0; e < 4; ++e)
               w[e] = f2_pack_bf16(f2_mul(f2_bits(o[c4 * 8 + 2 * e], o[c4 * 8 + 2 * e + 1]), inv2));
             const int chunk = q * 4 + c4;  // 16-byte chunk of the 256-byte row
-            const uint32_t addr = stage + (chunk >> 3) * (kTile / 2) + sw128_offset(rq, chunk & 7);
+            const uint32_t addr = stage + (chunk >> 3) * kHalf + sw128_offset(rq, chunk & 7);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
                          "r"(w[3])
                          : "memory");
@@ -356,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103_kernel(const __gri
         mbar_arrive(bar(B_OSTAGE + t));
         if (rq == 0) {
           if (mbar_wait(bar(B_OSTAGE + t), 0, lim)) {
-            tma_store_4d(&p.to[rl], stage, 0, hq, b, m * 128);
-            tma_store_4d(&p.to[rl], stage + kTile / 2, 64, hq, b, m * 128);
+            tma_store_4d(&p.to[rl], stage, 0, hq, b, q0);
+            tma_store_4d(&p.to[rl], stage + kHalf, 64, hq, b, q0);
             bulk_commit();
             bulk_wait_all();
           } else {
@@ -373,35 +390,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_sm103_kernel(const __gri
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // no remote arrive or multicast commit can target an exited CTA
   if (warp == 9) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc2(tmem, 512);
   }
 }
 
 }  // namespace
-
-// Query-tile schedule of a layer: key-tile range per query tile and the
-// order (most key tiles first). Host-side; the handle keeps device copies.
-void plan_tiles(const Layer& L, std::vector<int2>& kv_range, std::vector<int>& order) {
-  const int sl = (int)L.sl;
-  const int n_m = (sl + 127) / 128;
-  kv_range.resize(n_m);
-  std::vector<int> cost(n_m);
-  auto doc = [&](int t) {
-    return (int)(std::upper_bound(L.doc_offsets.begin(), L.doc_offsets.end(), t) - L.doc_offsets.begin()) - 1;
-  };
-  for (int m = 0; m < n_m; ++m) {
-    const int first = m * 128, last = std::min(sl, first + 128) - 1;
-    const int lo_key = L.doc_offsets[doc(first)];
-    const int hi_key = L.causal ? last : L.doc_offsets[doc(last) + 1] - 1;
-    kv_range[m] = make_int2(lo_key / 128, hi_key / 128);
-    cost[m] = kv_range[m].y - kv_range[m].x + 1;
-  }
-  order.resize(n_m);
-  std::iota(order.begin(), order.end(), 0);
-  std::stable_sort(order.begin(), order.end(), [&](int a, int c) { return cost[a] > cost[c]; });
-}
 
 bool fwd_sm103_supported(const Layer& L) { return L.dtype == ULYSSES_BF16 && L.hs == 128; }
 
@@ -414,11 +410,11 @@ int launch_attn_fwd_sm103(Layer& L, const void* const* q, const void* const* k, 
       return ULYSSES_ERR_CUDA;
     attr_set = true;
   }
-  const int n_m = (int)((L.sl + 127) / 128);
+  const int n_pair = (int)((L.sl + 255) / 256);
   const int group = L.Hq / L.Hk;
   FwdParams prm;
-  prm.kv_range = L.d_kv_range;
-  prm.m_order = L.d_m_order;
+  prm.kv_range = L.d_qp_range;
+  prm.m_order = L.d_qp_order;
   prm.doc_offsets = L.d_doc_offsets;
   prm.status = L.d_status;
   prm.timeout = L.timeout_cycles;
@@ -439,16 +435,16 @@ int launch_attn_fwd_sm103(Layer& L, const void* const* q, const void* const* k, 
     for (int i = 0; i < nr; ++i) {
       const int r = r0 + i;
       bool ok = make_tmap_bf16_4d(&prm.tq[i], q[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
-                make_tmap_bf16_4d(&prm.tk[i], k[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
+                make_tmap_bf16_4d(&prm.tk[i], k[r], 128, L.Hk, L.bs, L.sl, 64, 64) &&
                 make_tmap_bf16_4d(&prm.tv[i], v[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
                 make_tmap_bf16_4d(&prm.to[i], o[r], 128, L.Hq, L.bs, L.sl, 64, 128);
       if (!ok) return ULYSSES_ERR_CUDA;
       prm.lse[i] = lse[r];
     }
-    const long long grid = (long long)n_m * nr * L.bs * L.Hk * prm.npairs;
-    if (grid > 0x7fffffffLL) return ULYSSES_ERR_UNSUPPORTED;
+    const long long pairs = (long long)n_pair * nr * L.bs * L.Hk * prm.npairs;
+    if (2 * pairs > 0x7fffffffLL) return ULYSSES_ERR_UNSUPPORTED;
     Timed t(L.timing, ULYSSES_KERNEL_ATTN_FWD, stream);
-    attn_fwd_sm103_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(prm);
+    attn_fwd_sm103_kernel<<<(unsigned)(2 * pairs), kThreads, kSmemBytes, stream>>>(prm);
     t.done();
     count_launches(1);
     const cudaError_t e = cudaGetLastError();

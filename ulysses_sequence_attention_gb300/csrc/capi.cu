@@ -130,18 +130,9 @@ int ulysses_create(ulysses_t* out, int64_t sl, int64_t bs, int hc, int hkv, int 
     e = cudaMemcpy(L->d_doc_offsets, L->doc_offsets.data(), sizeof(int32_t) * (L->ndoc + 1),
                    cudaMemcpyHostToDevice);
   if (e == cudaSuccess && uly::fwd_sm103_supported(*L) && !L->empty()) {
-    std::vector<int2> kv_range;
-    std::vector<int> order;
-    uly::plan_tiles(*L, kv_range, order);
-    e = cudaMalloc(&L->d_kv_range, sizeof(int2) * kv_range.size());
-    if (e == cudaSuccess) e = cudaMalloc(&L->d_m_order, sizeof(int) * order.size());
-    if (e == cudaSuccess)
-      e = cudaMemcpy(L->d_kv_range, kv_range.data(), sizeof(int2) * kv_range.size(), cudaMemcpyHostToDevice);
-    if (e == cudaSuccess)
-      e = cudaMemcpy(L->d_m_order, order.data(), sizeof(int) * order.size(), cudaMemcpyHostToDevice);
     std::vector<int2> kvp, qp;
     std::vector<int> kvo, qo;
-    uly::plan_bwd_tiles(*L, kvp, kvo, qp, qo);
+    uly::plan_pair_tiles(*L, kvp, kvo, qp, qo);
     auto upload = [&](auto** dst, const auto& v) {
       using T = typename std::decay_t<decltype(v)>::value_type;
       if (e == cudaSuccess) e = cudaMalloc(dst, sizeof(T) * v.size());
@@ -155,8 +146,6 @@ int ulysses_create(ulysses_t* out, int64_t sl, int64_t bs, int hc, int hkv, int 
   if (e != cudaSuccess) {
     cudaFree(L->d_status);
     cudaFree(L->d_doc_offsets);
-    cudaFree(L->d_kv_range);
-    cudaFree(L->d_m_order);
     cudaFree(L->d_kvp_range);
     cudaFree(L->d_kvp_order);
     cudaFree(L->d_qp_range);
@@ -173,8 +162,6 @@ void ulysses_destroy(ulysses_t h) {
   if (!L) return;
   cudaFree(L->d_status);
   cudaFree(L->d_doc_offsets);
-  cudaFree(L->d_kv_range);
-  cudaFree(L->d_m_order);
   cudaFree(L->d_kvp_range);
   cudaFree(L->d_kvp_order);
   cudaFree(L->d_qp_range);

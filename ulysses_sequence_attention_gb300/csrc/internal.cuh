@@ -123,13 +123,10 @@ struct Layer {
   int32_t* d_doc_offsets = nullptr;   // device copy, ndoc + 1 entries
   unsigned* d_status = nullptr;       // device status word
   int device = 0;
-  // Tensor-core path: key-tile range per 128-row query tile, and the query
-  // tiles ordered by their number of key tiles (most first). Device copies.
-  int2* d_kv_range = nullptr;
-  int* d_m_order = nullptr;
-  // Backward (CTA pairs): per 256-key pair tile the range of query tiles that
-  // see it, per 256-query pair tile the range of key tiles it sees; both with
-  // an order by work.
+  // Tensor-core path (CTA pairs): per 256-key pair tile the range of 128-row
+  // query tiles that see it (dK/dV), per 256-query pair tile the range of
+  // 128-key tiles it sees (forward, dQ); each with an order by work, most
+  // first. Device copies.
   int2* d_kvp_range = nullptr;
   int* d_kvp_order = nullptr;
   int2* d_qp_range = nullptr;
@@ -182,12 +179,11 @@ int launch_attn_bwd_simt(const Layer& L, const void* const* q, const void* const
                          void* const* dv, void* workspace, cudaStream_t s);
 
 bool fwd_sm103_supported(const Layer& L);
-void plan_tiles(const Layer& L, std::vector<int2>& kv_range, std::vector<int>& order);
 int launch_attn_fwd_sm103(Layer& L, const void* const* q, const void* const* k, const void* const* v,
                           void* const* o, float* const* lse, cudaStream_t s);
 
-void plan_bwd_tiles(const Layer& L, std::vector<int2>& kv_pairs, std::vector<int>& kv_order,
-                    std::vector<int2>& q_pairs, std::vector<int>& q_order);
+void plan_pair_tiles(const Layer& L, std::vector<int2>& kv_pairs, std::vector<int>& kv_order,
+                     std::vector<int2>& q_pairs, std::vector<int>& q_order);
 size_t bwd_sm103_workspace(const Layer& L);
 int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* const* k, const void* const* v,
                           const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,

@@ -280,6 +280,22 @@ __device__ __forceinline__ void umma2_commit_both(uint32_t bar) {
       : "memory");
 }
 
+// Per-warp arrival on a barrier of the even CTA (remote from the odd one).
+__device__ __forceinline__ void warp_arrive_leader(uint32_t bar_local, uint32_t crank) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    if (crank == 0)
+      mbar_arrive(bar_local);
+    else
+      mbar_arrive_cluster(mapa(bar_local, 0));
+  }
+}
+__device__ __forceinline__ void warp_arrive_local(uint32_t bar_local) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar_local);
+}
+
+
 // Two fp32 -> packed bf16x2 (round to nearest even); lo goes to the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
