@@ -215,12 +215,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int st = jj % NS;
           const bool next = jj + 1 < n_kv;
           const int st1 = (jj + 1) % NS, u1 = (jj + 1) / NS;
-          if (next && !mbar_wait(bar(B_KVFULL + st1), u1 & 1, lim)) { ok = false; break; }
           for (int t = 0; t < ntile; ++t) {
             if (!mbar_wait(bar(B_PFULL + t), jj & 1, lim)) { ok = false; break; }
             tc_fence_after();
             issue_pv(t, st, jj > 0);
             if (next) {
+              if (t == 0) {
+                if (!mbar_wait(bar(B_KVFULL + st1), u1 & 1, lim)) { ok = false; break; }
+                tc_fence_after();
+              }
               issue_s(t, st1);  // over P of this tile: after the P V above has read it
               umma2_commit_both(bar(B_SFULL + t));
             }
@@ -293,9 +296,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (key < lo || key > hi) s[c] = __float_as_uint(-INFINITY);
           }
         }
-        float mx = -INFINITY;
+        // row max: four independent chains of three-input maxes
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+        for (int c = 0; c < 128; c += 8)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mq[j] = fmax3(mq[j], __uint_as_float(s[c + 2 * j]), __uint_as_float(s[c + 2 * j + 1]));
+        const float mx = fmax3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
         const float mx2 = mx * sl2;
         const bool need = mx2 > m_used + 8.0f;
         float alpha = 1.f;
