@@ -109,13 +109,12 @@ constexpr uint32_t kSmem = kOffBar + 256;
 enum {
   B_KV = 0,                  // K, V landed (even CTA: + the odd CTA's forward)
   B_QFULL = 1,               // NQ: query-half part (Qn, dOn) landed (even CTA: + 1 forward)
-  B_QEMPTY = B_QFULL + NQ,   // NQ: query-half part consumed by S^T, dP^T (commit, both CTAs)
+  B_QEMPTY = B_QFULL + NQ,   // NQ: query-half part consumed by S^T, dP^T (1 compute thread, this CTA)
   B_HFULL = B_QEMPTY + NQ,   // NQ: head-half part (Qh, dOh) landed (even CTA: + 1 forward)
   B_HEMPTY = B_HFULL + NQ,   // NQ: head-half part consumed by dV, dK (commit, both)
   B_S = B_HEMPTY + NQ,       // S^T ready (commit, both)
   B_DP = B_S + 1,            // dP^T ready (commit, both)
-  B_LOADED = B_DP + 1,       // this CTA's compute warps hold S^T, dP^T (8 warps)
-  B_P = B_LOADED + 1,        // even CTA: P^T, dS^T written in both CTAs (16 warps)
+  B_P = B_DP + 1,            // even CTA: P^T, dS^T written in both CTAs (16 warps)
   B_SFREE = B_P + 1,         // even CTA: S^T copied to registers in both CTAs (16 warps)
   B_DONE = B_SFREE + 1,      // every UMMA done (commit, both)
   B_EPI = B_DONE + 1,        // dK, dV staged (8 warps)
@@ -162,7 +161,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (i == B_KV || (i >= B_HFULL && i < B_HFULL + NQ) || (i >= B_QFULL && i < B_QFULL + NQ))
         cnt = crank == 0 ? 2 : 1;
       if (i >= B_RFULL && i < B_RFULL + NR) cnt = 32;
-      if (i == B_LOADED || i == B_EPI || (i >= B_REMPTY && i < B_REMPTY + NR)) cnt = 8;
+      if (i == B_EPI || (i >= B_REMPTY && i < B_REMPTY + NR)) cnt = 8;
       if (i == B_P || i == B_SFREE) cnt = 16;
       mbar_init(bar(i), cnt);
     }
@@ -276,7 +275,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           umma2_commit_both(bar(B_S));
           issue_dp(0);
           umma2_commit_both(bar(B_DP));
-          umma2_commit_both(bar(B_QEMPTY));
         }
         if (ok && n_it > 1) {
           ok = mbar_wait(bar(B_SFREE), 0, lim) && mbar_wait(bar(B_QFULL + 1 % NQ), (1 / NQ) & 1, lim);
@@ -302,16 +300,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {  // dV += P^T dO and dK += dS^T Q, interleaved
+            // query half kk/4 of P^T at 128 + 64 (kk/4), of dS^T 32 columns further
             const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-            umma2_ts(tmem + 256, tmem + 192 + kk * 8, b_mn(sq + 3 * kHalf, kk), id_tm, acc);
-            umma2_ts(tmem + 384, tmem + 128 + kk * 8, b_mn(sq + 2 * kHalf, kk), id_tm, acc);
+            const uint32_t a = tmem + 128 + (kk >> 2) * 64 + (kk & 3) * 8;
+            umma2_ts(tmem + 256, a, b_mn(sq + 3 * kHalf, kk), id_tm, acc);
+            umma2_ts(tmem + 384, a + 32, b_mn(sq + 2 * kHalf, kk), id_tm, acc);
           }
           umma2_commit_both(bar(B_HEMPTY + st));
           if (it + 1 < n_it) {
-            const int st1 = (it + 1) % NQ;
-            issue_dp(st1);  // its query part landed before S_{i+1} was issued
+            issue_dp((it + 1) % NQ);  // its query part landed before S_{i+1} was issued
             umma2_commit_both(bar(B_DP));
-            umma2_commit_both(bar(B_QEMPTY + st1));  // the query part of tile i+1 is consumed
           }
           if (it + 2 < n_it) {
             const int st2 = (it + 2) % NQ;
@@ -406,23 +404,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DP), it & 1, lim));
       if (!ok) break;
       tc_fence_after();
+      if (warp == 0 && lane == 0) {
+        // dP^T of tile it has completed, and with it S^T: the query part of
+        // its stage is free for the producer. (The head part is released by
+        // a commit right after dV/dK, which is earlier.)
+        mbar_arrive(bar(B_QEMPTY + it % NQ));
+      }
+      __syncwarp();
       uint32_t dp[64];
       tmem_ld32(tmem + lane_base + 128 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
       tmem_ld32(tmem + lane_base + 160 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
       tmem_ld_wait();
-      tc_fence_before();
-      warp_arrive_local(bar(B_LOADED));  // both halves read before either is overwritten
       // dS^T = P^T * (dP^T - D)
       const uint64_t* d2 = reinterpret_cast<const uint64_t*>(rs + 128 + 64 * h);
       uint32_t dk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) dk[c] = f2_pack_bf16(f2_mul(pp[c], f2_sub(f2_bits(dp[2 * c], dp[2 * c + 1]), d2[c])));
       warp_arrive_local(bar(B_REMPTY + rsl));  // done with this tile's LSE/D rows
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_LOADED), it & 1, lim));
-      if (!ok) break;
-      tc_fence_after();
-      tmem_st32(tmem + lane_base + 192 + 32 * h, pk);  // P^T (bf16), over dP^T
-      tmem_st32(tmem + lane_base + 128 + 32 * h, dk);  // dS^T (bf16), over dP^T
+      // P^T and dS^T (bf16) over the dP^T columns this thread has just read:
+      // no other thread reads them
+      tmem_st32(tmem + lane_base + 128 + 64 * h, pk);
+      tmem_st32(tmem + lane_base + 160 + 64 * h, dk);
       tmem_st_wait();
       tc_fence_before();
       warp_arrive_leader(bar(B_P), crank);
@@ -488,11 +490,10 @@ constexpr uint32_t kSmem = kOffBar + 256;
 enum {
   B_QO = 0,                  // Q, dO landed (even CTA: + forward)
   B_KFULL = 1,               // NK: key stage landed (even CTA: + forward)
-  B_KEMPTY = B_KFULL + NK,   // NK: key stage consumed (commit, both)
+  B_KEMPTY = B_KFULL + NK,   // NK: key stage consumed (1 compute thread, this CTA)
   B_S = B_KEMPTY + NK,       // 2: S ready in buffer 0 / 1 (commit, both)
   B_DP = B_S + 2,            // dP ready (commit, both)
-  B_LOADED = B_DP + 1,       // this CTA's compute warps hold dP (8 warps)
-  B_DS = B_LOADED + 1,       // even CTA: dS written in both CTAs (16 warps)
+  B_DS = B_DP + 1,           // even CTA: dS written in both CTAs (16 warps)
   B_DONE = B_DS + 1,         // every UMMA done (commit, both)
   B_EPI = B_DONE + 1,        // dQ staged (8 warps)
   B_DRAIN = B_EPI + 1,
@@ -533,7 +534,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
       if (i == B_QO || (i >= B_KFULL && i < B_KFULL + NK)) cnt = crank == 0 ? 2 : 1;
-      if (i == B_LOADED || i == B_EPI) cnt = 8;
+      if (i == B_EPI) cnt = 8;
       if (i == B_DS) cnt = 16;
       mbar_init(bar(i), cnt);
     }
@@ -633,9 +634,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t sk = sb + kOffStage + st * kStage;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dQ += dS K
-            umma2_ts(tmem + 384, tmem + 256 + kk * 8, b_mn(sk + 2 * kHalf, kk), id_tm, (jj > 0 || kk > 0) ? 1u : 0u);
-          umma2_commit_both(bar(B_KEMPTY + st));
+          for (int kk = 0; kk < 8; ++kk)  // dQ += dS K; key half kk/4 of dS at 256 + 64 (kk/4)
+            umma2_ts(tmem + 384, tmem + 256 + (kk >> 2) * 64 + (kk & 3) * 8, b_mn(sk + 2 * kHalf, kk), id_tm,
+                     (jj > 0 || kk > 0) ? 1u : 0u);
           if (next) issue_dp(jj + 1);  // overwrites dS only after dQ has read it (issue order)
         }
         if (ok)
@@ -708,19 +709,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DP), jj & 1, lim));
       if (!ok) break;
       tc_fence_after();
+      // dP of key tile jj has completed, and with it dQ of tile jj-1: that
+      // tile's key stage is free for the producer.
+      if (warp == 0 && lane == 0 && jj > 0) mbar_arrive(bar(B_KEMPTY + (jj - 1) % NK));
+      __syncwarp();
       uint32_t dp[64];
       tmem_ld32(tmem + lane_base + 256 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
       tmem_ld32(tmem + lane_base + 288 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
       tmem_ld_wait();
-      tc_fence_before();
-      warp_arrive_local(bar(B_LOADED));
       uint32_t dk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) dk[c] = f2_pack_bf16(f2_mul(pp[c], f2_sub(f2_bits(dp[2 * c], dp[2 * c + 1]), D2)));
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_LOADED), jj & 1, lim));
-      if (!ok) break;
-      tc_fence_after();
-      tmem_st32(tmem + lane_base + 256 + 32 * h, dk);  // dS (bf16) over dP
+      tmem_st32(tmem + lane_base + 256 + 64 * h, dk);  // dS (bf16) over the dP columns this thread read
       tmem_st_wait();
       tc_fence_before();
       warp_arrive_leader(bar(B_DS), crank);

@@ -90,7 +90,7 @@ struct FwdParams {
 enum {
   B_QFULL = 0,               // Q landed (even CTA: + the odd CTA's forward)
   B_KVFULL = 1,              // NS: K/V halves landed (even CTA: + forward)
-  B_KVEMPTY = B_KVFULL + NS, // NS: stage consumed (commit, both CTAs)
+  B_KVEMPTY = B_KVFULL + NS, // NS: stage consumed (1 softmax thread, this CTA)
   B_SFULL = B_KVEMPTY + NS,  // 2: S of tile t ready (commit, both)
   B_PFULL = B_SFULL + 2,     // 2: even CTA: P of tile t written in both CTAs (8 warps)
   B_OFINAL = B_PFULL + 2,    // 2: every UMMA of tile t done (commit, both)
@@ -229,7 +229,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          umma2_commit_both(bar(B_KVEMPTY + st));
         }
         if (ok) {
           for (int t = 0; t < ntile; ++t) umma2_commit_both(bar(B_OFINAL + t));
@@ -282,6 +281,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL + t), jj & 1, lim));
         if (!ok) break;
         tc_fence_after();
+        // S of the last tile for key tile jj is the last UMMA issued for key
+        // tile jj-1: once it has completed, that tile's K/V stage is free.
+        if (t == ntile - 1 && rq == 0 && jj > 0) mbar_arrive(bar(B_KVEMPTY + (jj - 1) % NS));
+        __syncwarp();
         uint32_t s[128];
         tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
         tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
