@@ -112,8 +112,11 @@ const char* ulysses_strerror(int status);
 
 /*
  * ulysses_workspace_size — bytes of device workspace that ulysses_attn_bwd needs.
- * Layout: for each rank, the fp32 rows D = rowsum(dO * O), [bs][hc/P][sl]
- * (P * bs * hc * sl * 4 bytes in all). Pure host computation.
+ * bf16 with hs = 128 (the tensor-core path): for each rank, two fp32 row
+ * planes [bs][hc/P][pitch], -LSE*log2(e) and D = rowsum(dO * O), where pitch
+ * is sl rounded up to a multiple of 4: P * 2 * bs * (hc/P) * pitch * 4 bytes.
+ * Other configurations: D only, P * bs * (hc/P) * sl * 4 bytes. Pure host
+ * computation.
  */
 int ulysses_workspace_size(ulysses_t h, size_t* bytes);
 
@@ -288,14 +291,14 @@ int ulysses_timing_read(ulysses_t h, int kernel, double* total_ms, int64_t* laun
  * Limits and sharing:
  *  - A layer whose backward needs more than ULYSSES_NOALLOC_SCRATCH_BYTES of
  *    workspace (see ulysses_workspace_size) is rejected with
- *    ULYSSES_ERR_TOO_LARGE before anything is enqueued. The workspace is 4
- *    bytes per (token, query head, batch element): 64 MiB covers, for example,
- *    512K tokens of a 32-query-head layer.
+ *    ULYSSES_ERR_TOO_LARGE before anything is enqueued. The workspace is 8
+ *    bytes per (token, query head, batch element) on the tensor-core path:
+ *    64 MiB covers, for example, 256K tokens of a 32-query-head layer.
  *  - Every call shares the one array, and it keeps the last call's contents.
  *    Each call clears the parts that must start at zero itself. Two calls that
  *    overlap on the GPU (on different streams, or different host threads
- *    without ordering) race on the array and corrupt each other's dQ: order
- *    them.
+ *    without ordering) race on the array and corrupt each other's gradients:
+ *    order them.
  *  - The first call on a device looks up the array's device address with
  *    cudaGetSymbolAddress (once per device, with that device current). Make
  *    that first call before any stream capture begins.

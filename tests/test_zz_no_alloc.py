@@ -77,8 +77,8 @@ def test_noalloc_matches_the_allocating_entry_point(u, sl, hc, hkv, P, offs):
 
 
 def test_noalloc_rejects_a_layer_beyond_its_scratch(u):
-    # D rows need 4 bytes per (token, query head, batch element):
-    # 256 tokens x 2 heads x 65535 batch = 128 MiB > 64 MiB. The size check
+    # The row planes need 8 bytes per (token, query head, batch element):
+    # 256 tokens x 2 heads x 65535 batch = 256 MiB > 64 MiB. The size check
     # comes before any pointer is looked at, so no buffers are needed.
     h = u.ulysses_create(256, 65535, 2, 2, 128, 1, True, None, torch.bfloat16)
     assert u.ulysses_workspace_size(h) > u.ULYSSES_NOALLOC_SCRATCH_BYTES

@@ -67,14 +67,15 @@ struct PairParams {
   CUtensorMap tf[kRanksPerLaunch];   // dkdv: dO 64x128    dq: dQ (store)
   CUtensorMap tg[kRanksPerLaunch];   // dkdv: dK (store)
   CUtensorMap th[kRanksPerLaunch];   // dkdv: dV (store)
-  const float* lse[kRanksPerLaunch];
-  const float* D[kRanksPerLaunch];   // [bs][Hq][sl]
+  CUtensorMap tr[kRanksPerLaunch];   // dkdv: the row planes (-LSE log2 e, D) of a rank, boxes of 128 x 1 x 2
+  const float* rows[kRanksPerLaunch];  // dq: the row planes of a rank, [2][bs*Hq][pitch]
   const int2* range;                 // per pair tile: first and last tile of the other side
   const int* order;                  // pair tiles, most work first
   const int32_t* doc_offsets;
   unsigned* status;
   long long timeout;
   int ndoc, sl, bs, Hq, Hk, group, nranks, causal;
+  int pitch;                         // floats per row of a row plane (sl rounded up to 4)
   float scale, scale_log2;
 };
 
@@ -119,7 +120,7 @@ enum {
   B_DONE = B_SFREE + 1,      // every UMMA done (commit, both)
   B_EPI = B_DONE + 1,        // dK, dV staged (8 warps)
   B_DRAIN = B_EPI + 1,
-  B_RFULL = B_DRAIN + 1,     // NR: LSE/D rows written (32 lanes, this CTA)
+  B_RFULL = B_DRAIN + 1,     // NR: -LSE/D rows landed (TMA, this CTA)
   B_REMPTY = B_RFULL + NR,   // NR: rows read by this CTA's compute warps (8 warps)
   B_COUNT = B_REMPTY + NR
 };
@@ -160,7 +161,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t cnt = 1;
       if (i == B_KV || (i >= B_HFULL && i < B_HFULL + NQ) || (i >= B_QFULL && i < B_QFULL + NQ))
         cnt = crank == 0 ? 2 : 1;
-      if (i >= B_RFULL && i < B_RFULL + NR) cnt = 32;
       if (i == B_EPI || (i >= B_REMPTY && i < B_REMPTY + NR)) cnt = 8;
       if (i == B_P || i == B_SFREE) cnt = 16;
       mbar_init(bar(i), cnt);
@@ -183,8 +183,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 8) {
       // --------------------------------------------------------- TMA producer
       bool ok = true;
-      int last[NQ], last_h[NQ];
+      int last[NQ], last_h[NQ], last_r[NR];
       for (int i = 0; i < NQ; ++i) last[i] = last_h[i] = -1;
+      for (int i = 0; i < NR; ++i) last_r[i] = -1;
       if (lane == 0) {
         mbar_expect_tx(bar(B_KV), 2 * kTile);
         tma_load_4d(sb + kOffK, &p.ta[rl], bar(B_KV), 0, hk, b, kv0);
@@ -198,21 +199,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int m = qr.x + it % nm;
         const uint32_t sq = sb + kOffStage + st * kStage;
         const int q0 = m * 128;
-        // -LSE (log2 units) and D rows of the tile; rows past the end get
-        // -LSE = -inf, so that P = 0 there.
+        // -LSE (log2 units) and D of the tile's 128 query rows, one TMA box
+        // from the two row planes. Rows past sl read as zero; every key masks
+        // them, so P = 0 there and dS = 0.
         const int rsl = it % NR;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(B_REMPTY + rsl), ((it / NR) & 1) ^ 1, lim));
         if (!ok) break;
-        float* rs = rows + rsl * 256;
-        const size_t base = ((size_t)b * p.Hq + hq) * p.sl;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = q0 + lane * 4 + e;
-          const bool in = i < p.sl;
-          rs[lane * 4 + e] = in ? -(p.lse[rl][base + i] * 1.4426950408889634f) : -INFINITY;
-          rs[128 + lane * 4 + e] = in ? p.D[rl][base + i] : 0.f;
+        if (lane == 0) {
+          mbar_expect_tx(bar(B_RFULL + rsl), 1024);
+          tma_load_3d(sb + kOffRow + rsl * 1024, &p.tr[rl], bar(B_RFULL + rsl), q0, b * p.Hq + hq, 0);
         }
-        mbar_arrive(bar(B_RFULL + rsl));
+        last_r[rsl] = it / NR;
         // query-half part: Q and dO rows [q0 + 64c, +64) (B of S^T, dP^T: N = queries)
         ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QEMPTY + st), (u & 1) ^ 1, lim));
         if (!ok) break;
@@ -242,6 +239,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (last[i] >= 0) mbar_wait(bar(B_QFULL + i), last[i] & 1, lim);
           if (last_h[i] >= 0) mbar_wait(bar(B_HFULL + i), last_h[i] & 1, lim);
         }
+        for (int i = 0; i < NR; ++i)
+          if (last_r[i] >= 0) mbar_wait(bar(B_RFULL + i), last_r[i] & 1, lim);
       }
       __syncwarp();
     } else if (warp == 9 && crank == 0) {
@@ -669,17 +668,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int iq = quarter * 32 + lane;      // query row within this CTA = TMEM lane
     const int i = q0 + iq;                   // global query position
     int klo = 1, khi = 0;                    // keys visible from query i: [klo, khi]
-    float lse2 = INFINITY, Di = 0.f;
+    float nl2 = -INFINITY, Di = 0.f;  // -LSE (log2 units) and D of row i
     if (i < p.sl) {
       const int d = doc_of(p.doc_offsets, p.ndoc, i);
       klo = p.doc_offsets[d];
       khi = p.causal ? i : p.doc_offsets[d + 1] - 1;
-      const size_t base = ((size_t)b * p.Hq + hq) * p.sl + i;
-      lse2 = p.lse[rl][base] * 1.4426950408889634f;
-      Di = p.D[rl][base];
+      const size_t plane = (size_t)p.bs * p.Hq * p.pitch;
+      const size_t base = ((size_t)b * p.Hq + hq) * p.pitch + i;
+      nl2 = p.rows[rl][base];
+      Di = p.rows[rl][plane + base];
     }
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const uint64_t sc2 = f2(p.scale_log2, p.scale_log2), nl2 = f2(-lse2, -lse2), D2 = f2(Di, Di);
+    const uint64_t sc2 = f2(p.scale_log2, p.scale_log2), nlp = f2(nl2, nl2), D2 = f2(Di, Di);
     bool ok = true;
     for (int jj = 0; jj < n_kv; ++jj) {
       const int k0 = (kr.x + jj) * 128 + 64 * h;
@@ -694,7 +694,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool full = klo <= k0 && k0 + 63 <= khi;
       uint64_t pp[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) pp[c] = f2_ex2(f2_fma(f2_bits(pf[2 * c], pf[2 * c + 1]), sc2, nl2));
+      for (int c = 0; c < 32; ++c) pp[c] = f2_ex2(f2_fma(f2_bits(pf[2 * c], pf[2 * c + 1]), sc2, nlp));
       if (!full) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
@@ -764,12 +764,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
-// D = rowsum(dO * O) for every (rank, batch, head, row). 16 lanes per row.
+// The row planes of the backward, for every (rank, batch, head, row):
+// -LSE * log2(e) (plane 0) and D = rowsum(dO * O) (plane 1), each
+// [bs][Hq][pitch] fp32. 16 lanes per row.
 struct PrepParams {
   const __nv_bfloat16* o[ULYSSES_MAX_P];
   const __nv_bfloat16* dO[ULYSSES_MAX_P];
-  float* D[ULYSSES_MAX_P];
-  int P, sl, bs, Hq;
+  const float* lse[ULYSSES_MAX_P];
+  float* rows[ULYSSES_MAX_P];
+  int P, sl, bs, Hq, pitch;
   long long rows_per_rank;  // sl * bs * Hq
 };
 
@@ -801,12 +804,17 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constan
     }
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (active && part == 0) {
+    if (active && part < 2) {
       const int hq = (int)(rr % a.Hq);
       const long long tb = rr / a.Hq;
       const int bb = (int)(tb % a.bs);
       const long long t = tb / a.bs;
-      a.D[r][((long long)bb * a.Hq + hq) * a.sl + t] = acc;
+      const long long plane = (long long)a.bs * a.Hq * a.pitch;
+      const long long at = ((long long)bb * a.Hq + hq) * a.pitch + t;
+      if (part == 0)
+        a.rows[r][plane + at] = acc;
+      else
+        a.rows[r][at] = -(a.lse[r][((long long)bb * a.Hq + hq) * a.sl + t] * 1.4426950408889634f);
     }
   }
 }
@@ -847,7 +855,8 @@ void plan_pair_tiles(const Layer& L, std::vector<int2>& kv_pairs, std::vector<in
   order_by(q_pairs, q_order);
 }
 
-size_t bwd_sm103_workspace(const Layer& L) { return (size_t)L.P * L.bs * L.Hq * L.sl * sizeof(float); }
+int64_t bwd_row_pitch(const Layer& L) { return (L.sl + 3) / 4 * 4; }
+size_t bwd_sm103_workspace(const Layer& L) { return (size_t)L.P * 2 * L.bs * L.Hq * bwd_row_pitch(L) * sizeof(float); }
 
 static int grid_cap(long long work) {
   long long g = (work + 255) / 256;
@@ -866,21 +875,27 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
       return ULYSSES_ERR_CUDA;
     attr_set = true;
   }
-  float* D_base = reinterpret_cast<float*>(workspace);
-  const long long per_rank_D = (long long)L.bs * L.Hq * L.sl;
+  // Workspace: per rank two row planes, -LSE*log2(e) then D, each
+  // [bs*Hq][pitch] fp32 with the pitch a multiple of 16 bytes (a TMA stride).
+  float* ws = reinterpret_cast<float*>(workspace);
+  const long long pitch = bwd_row_pitch(L);
+  const long long nrows = (long long)L.bs * L.Hq;
+  const long long per_rank = 2 * nrows * pitch;
 
-  // 1. D = rowsum(dO * O).
+  // 1. The row planes.
   {
     PrepParams a;
     for (int r = 0; r < L.P; ++r) {
       a.o[r] = reinterpret_cast<const __nv_bfloat16*>(o[r]);
       a.dO[r] = reinterpret_cast<const __nv_bfloat16*>(dO[r]);
-      a.D[r] = D_base + per_rank_D * r;
+      a.lse[r] = lse[r];
+      a.rows[r] = ws + per_rank * r;
     }
     a.P = L.P;
     a.sl = (int)L.sl;
     a.bs = (int)L.bs;
     a.Hq = L.Hq;
+    a.pitch = (int)pitch;
     a.rows_per_rank = (long long)L.sl * L.bs * L.Hq;
     Timed t(L.timing, ULYSSES_KERNEL_BWD_PREP, stream);
     attn_bwd_prep_kernel<<<grid_cap(a.rows_per_rank * L.P * 16), 256, 0, stream>>>(a);
@@ -898,6 +913,7 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
   prm.Hk = L.Hk;
   prm.group = L.Hq / L.Hk;
   prm.causal = L.causal;
+  prm.pitch = (int)pitch;
   prm.scale = (float)(1.0 / sqrt((double)L.hs));
   prm.scale_log2 = (float)(1.4426950408889634 / sqrt((double)L.hs));
   const int n_pair = (int)((L.sl + 255) / 256);
@@ -918,7 +934,9 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
                make_tmap_bf16_4d(&prm.te[i], q[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
                make_tmap_bf16_4d(&prm.tf[i], dO[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
                make_tmap_bf16_4d(&prm.tg[i], dk[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
-               make_tmap_bf16_4d(&prm.th[i], dv[r], 128, L.Hk, L.bs, L.sl, 64, 128);
+               make_tmap_bf16_4d(&prm.th[i], dv[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
+               make_tmap_f32_rows(&prm.tr[i], ws + per_rank * r, (uint64_t)L.sl, (uint64_t)nrows,
+                                  (uint64_t)pitch);
         else
           ok = make_tmap_bf16_4d(&prm.ta[i], q[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
                make_tmap_bf16_4d(&prm.tb[i], dO[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
@@ -927,8 +945,7 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
                make_tmap_bf16_4d(&prm.te[i], k[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
                make_tmap_bf16_4d(&prm.tf[i], dq[r], 128, L.Hq, L.bs, L.sl, 64, 128);
         if (!ok) return ULYSSES_ERR_CUDA;
-        prm.lse[i] = lse[r];
-        prm.D[i] = D_base + per_rank_D * r;
+        prm.rows[i] = ws + per_rank * r;
       }
       const long long pairs = (long long)n_pair * nr * L.bs * (pass == 0 ? L.Hk : L.Hq);
       if (2 * pairs > 0x7fffffffLL) return ULYSSES_ERR_UNSUPPORTED;

@@ -172,8 +172,11 @@ void ulysses_destroy(ulysses_t h) {
 int ulysses_workspace_size(ulysses_t h, size_t* bytes) {
   const Layer* L = reinterpret_cast<const Layer*>(h);
   if (!L || !bytes) return ULYSSES_ERR_INVALID_ARG;
-  // The fp32 rows D = rowsum(dO * O): [P][bs][Hq][sl].
-  *bytes = (size_t)L->P * L->bs * L->Hq * L->sl * sizeof(float);
+  // Tensor-core path: per rank two fp32 row planes, -LSE*log2(e) and
+  // D = rowsum(dO * O), [bs][Hq][sl rounded up to 4] each. Other paths: D only,
+  // [P][bs][Hq][sl].
+  *bytes = uly::fwd_sm103_supported(*L) ? uly::bwd_sm103_workspace(*L)
+                                        : (size_t)L->P * L->bs * L->Hq * L->sl * sizeof(float);
   return ULYSSES_OK;
 }
 

@@ -11,9 +11,10 @@
 
 namespace {
 
-// The workspace of ulysses_attn_bwd_noalloc: the fp32 dQ accumulators and the
-// D rows. It lives for the lifetime of the process on every device that loads
-// the library. Calls share it; the backward zeroes the accumulators itself.
+// The workspace of ulysses_attn_bwd_noalloc: the backward's fp32 row planes
+// (-LSE*log2(e) and D). It lives for the lifetime of the process on every
+// device that loads the library. Calls share it; each backward writes the
+// rows before it reads them.
 static __device__ __align__(256) unsigned char g_bwd_scratch[ULYSSES_NOALLOC_SCRATCH_BYTES];
 
 // Device address of g_bwd_scratch for each device. In host code the symbol is

@@ -61,6 +61,22 @@ inline bool make_tmap_f32_4d(CUtensorMap* map, const void* base, uint64_t d0, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The two fp32 row planes of the backward, [2][nrows][pitch] (pitch a
+// multiple of 4 floats; only the first `len` floats of a row are in the
+// tensor, so reads past them return zero), in boxes of 128 x 1 x 2: the same
+// 128 rows of both planes land as [plane][128] floats.
+inline bool make_tmap_f32_rows(CUtensorMap* map, const void* base, uint64_t len, uint64_t nrows, uint64_t pitch) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn || pitch % 4 != 0) return false;
+  const cuuint64_t dims[3] = {len, nrows, 2};
+  const cuuint64_t strides[2] = {pitch * 4, nrows * pitch * 4};
+  const cuuint32_t box[3] = {128, 1, 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // A rank-2 bf16 tensor [d1][d0], boxes of box0 x box1, 128-byte swizzle.
 inline bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint32_t box0,
                               uint32_t box1) {
