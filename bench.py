@@ -10,6 +10,13 @@ One step is the whole hot path on one batch of seeded synthetic input:
 Llama-8B-shaped forward+backward layer at sl=32768: P=8 virtual ranks, 32 query
 heads, 8 kv heads, head size 128, bf16, causal.
 
+Where the shape allows it (``--path auto``, the default), the step runs the
+fused entry points ulysses_layer_fwd / ulysses_layer_bwd: the exchanges happen
+inside the attention kernels, which read and write the sequence shards through
+their TMA tensor maps. ``--path explicit`` runs the exchange kernels between
+the attention calls instead. Either way the exchange kernels are also timed in
+a loop of their own, for the exchange GB/s part of the metric.
+
 Output: one JSON line on rank 0. ``value`` is tokens/s over the whole job,
 timed with CUDA events with inputs already resident in HBM. ``e2e`` is the
 same metric through the public API, with the host->device copy of the step's
@@ -196,12 +203,12 @@ def run_ours(args, w, rank, world):
     x = make_global_inputs(w)
     P = w.P
     seq = {k: [t.to(dev) for t in split_shards(v, P)] for k, v in x.items()}
-    L = U.UlyssesLayer(w.sl, w.bs, w.hc, w.hkv, w.hs, P, w.causal, offs, w.torch_dtype, device=str(dev))
+    fused = None if args.path == "auto" else args.path == "fused"
+    L = U.UlyssesLayer(w.sl, w.bs, w.hc, w.hkv, w.hs, P, w.causal, offs, w.torch_dtype, device=str(dev),
+                       fused=fused)
     o = L.new_seq_shards(w.hc)
     if w.backward:
         dq, dk, dv = L.new_seq_shards(w.hc), L.new_seq_shards(w.hkv), L.new_seq_shards(w.hkv)
-    L._alloc(backward=w.backward)
-    b = L.head_buffers
     h = L.h
     stream = torch.cuda.current_stream(dev)
     ev = {}
@@ -211,37 +218,75 @@ def run_ours(args, w, rank, world):
         e.record(stream)
         ev.setdefault(name, []).append(e)
 
+    def heads(H):
+        return [torch.empty((w.sl, w.bs, H, w.hs), dtype=w.torch_dtype, device=dev) for _ in range(P)]
+
+    # Head-shard buffers: the explicit path's intermediates, and the targets of
+    # the exchange measurement on either path.
+    hb = {"qh": heads(L.Hq), "kh": heads(L.Hk), "vh": heads(L.Hk), "oh": heads(L.Hq)}
+    if w.backward:
+        hb.update(doh=heads(L.Hq), dqh=heads(L.Hq), dkh=heads(L.Hk), dvh=heads(L.Hk))
+    lse = [torch.empty((w.bs, L.Hq, w.sl), dtype=torch.float32, device=dev) for _ in range(P)]
+    ws = torch.empty((max(B.ulysses_workspace_size(h), 16) + 3) // 4, dtype=torch.float32, device=dev)
+
     def step(timed):
-        if timed:
-            mark("s2h0")
-        B.ulysses_seq_to_head(h, w.hc, seq["q"], b["qh"])
-        B.ulysses_seq_to_head(h, w.hkv, seq["k"], b["kh"])
-        B.ulysses_seq_to_head(h, w.hkv, seq["v"], b["vh"])
+        """One pass of the whole hot path on resident inputs."""
+        if L.fused:
+            if timed:
+                mark("fwd0")
+            B.ulysses_layer_fwd(h, seq["q"], seq["k"], seq["v"], o, lse)
+            if timed:
+                mark("fwd1")
+            if w.backward:
+                B.ulysses_layer_bwd(h, seq["q"], seq["k"], seq["v"], o, seq["do"], lse, dq, dk, dv, ws)
+                if timed:
+                    mark("bwd1")
+            return
         if timed:
             mark("fwd0")
-        B.ulysses_attn_fwd(h, b["qh"], b["kh"], b["vh"], b["oh"], b["lse"])
+        B.ulysses_seq_to_head(h, w.hc, seq["q"], hb["qh"])
+        B.ulysses_seq_to_head(h, w.hkv, seq["k"], hb["kh"])
+        B.ulysses_seq_to_head(h, w.hkv, seq["v"], hb["vh"])
+        B.ulysses_attn_fwd(h, hb["qh"], hb["kh"], hb["vh"], hb["oh"], lse)
+        B.ulysses_head_to_seq(h, w.hc, hb["oh"], o)
         if timed:
             mark("fwd1")
-        B.ulysses_head_to_seq(h, w.hc, b["oh"], o)
-        if timed:
-            mark("h2s1")
         if w.backward:
-            B.ulysses_seq_to_head(h, w.hc, seq["do"], b["doh"])
-            if timed:
-                mark("bwd0")
-            B.ulysses_attn_bwd(h, b["qh"], b["kh"], b["vh"], b["oh"], b["doh"], b["lse"],
-                               b["dqh"], b["dkh"], b["dvh"], b["ws"])
+            B.ulysses_seq_to_head(h, w.hc, seq["do"], hb["doh"])
+            B.ulysses_attn_bwd(h, hb["qh"], hb["kh"], hb["vh"], hb["oh"], hb["doh"], lse,
+                               hb["dqh"], hb["dkh"], hb["dvh"], ws)
+            B.ulysses_head_to_seq(h, w.hc, hb["dqh"], dq)
+            B.ulysses_head_to_seq(h, w.hkv, hb["dkh"], dk)
+            B.ulysses_head_to_seq(h, w.hkv, hb["dvh"], dv)
             if timed:
                 mark("bwd1")
-            B.ulysses_head_to_seq(h, w.hc, b["dqh"], dq)
-            B.ulysses_head_to_seq(h, w.hkv, b["dkh"], dk)
-            B.ulysses_head_to_seq(h, w.hkv, b["dvh"], dv)
-        if timed:
-            mark("end")
+
+    def exchange_step():
+        """The explicit exchanges of one step: Q, K, V (and dO) seq->head, O (and dQ, dK, dV) head->seq."""
+        mark("x0")
+        B.ulysses_seq_to_head(h, w.hc, seq["q"], hb["qh"])
+        B.ulysses_seq_to_head(h, w.hkv, seq["k"], hb["kh"])
+        B.ulysses_seq_to_head(h, w.hkv, seq["v"], hb["vh"])
+        mark("x1")
+        B.ulysses_head_to_seq(h, w.hc, hb["oh"], o)
+        mark("x2")
+        if w.backward:
+            B.ulysses_seq_to_head(h, w.hc, seq["do"], hb["doh"])
+            B.ulysses_head_to_seq(h, w.hc, hb["dqh"], dq)
+            B.ulysses_head_to_seq(h, w.hkv, hb["dkh"], dk)
+            B.ulysses_head_to_seq(h, w.hkv, hb["dvh"], dv)
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
+
+    def read_timing():
+        out = {}
+        for i, name in enumerate(U.KERNEL_NAMES):
+            ms, n = U.ulysses_timing_read(h, i)
+            if n:
+                out[name] = {"total_ms": ms, "launches": n, "ms_per_step": ms / args.steps}
+        return out
 
     for _ in range(args.warmup):
         step(False)
@@ -265,24 +310,36 @@ def run_ours(args, w, rank, world):
     torch.cuda.synchronize(dev)
     barrier()
     launches = U.ulysses_launch_count() - n0
+    kernels = read_timing()
     U.ulysses_timing_enable(h, False)
-    kernels = {}
-    for i, name in enumerate(U.KERNEL_NAMES):
-        ms, n = U.ulysses_timing_read(h, i)
-        if n:
-            kernels[name] = {"total_ms": ms, "launches": n, "ms_per_step": ms / args.steps}
     clk = clocks.stop()
     elapsed_ms = t0.elapsed_time(t1)
     if U.ulysses_get_status(h) != U.ULYSSES_OK:
         raise RuntimeError("device status after the timed region is not OK")
 
+    # The exchange kernels, timed on their own (on the fused path the step
+    # runs none: the attention kernels read and write the sequence shards).
+    for _ in range(3):
+        exchange_step()
+    torch.cuda.synchronize(dev)
+    ev.pop("x0", None), ev.pop("x1", None), ev.pop("x2", None)
+    U.ulysses_timing_enable(h, True)
+    for _ in range(args.steps):
+        exchange_step()
+    torch.cuda.synchronize(dev)
+    xk = read_timing()
+    U.ulysses_timing_enable(h, False)
+    for name in ("seq_to_head", "head_to_seq"):
+        if name in xk:
+            kernels.setdefault(name, dict(xk[name], region="exchange-only loop of the same step's exchanges"))
+
     def span(a, z):
         return [ea.elapsed_time(ez) for ea, ez in zip(ev[a], ev[z])]
 
     fwd_ms = statistics.mean(span("fwd0", "fwd1"))
-    s2h_ms = statistics.mean(span("s2h0", "fwd0"))
-    h2s_ms = statistics.mean(span("fwd1", "h2s1"))
-    bwd_ms = statistics.mean(span("bwd0", "bwd1")) if w.backward else 0.0
+    bwd_ms = statistics.mean(span("fwd1", "bwd1")) if w.backward else 0.0
+    s2h_ms = statistics.mean(span("x0", "x1"))
+    h2s_ms = statistics.mean(span("x1", "x2"))
 
     # max over ranks
     t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
@@ -299,7 +356,7 @@ def run_ours(args, w, rank, world):
 
     result = {"ms_per_step": ms_per_step, "value": value, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
               "s2h_qkv_ms": s2h_ms, "h2s_o_ms": h2s_ms, "launches": launches, "clocks": clk, "e2e": e2e,
-              "kernels": kernels}
+              "kernels": kernels, "path": "fused" if L.fused else "explicit"}
     return result
 
 
@@ -423,6 +480,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama8b_32k", choices=sorted(WORKLOADS))
+    ap.add_argument("--path", choices=["auto", "fused", "explicit"], default="auto",
+                    help="fused: exchanges inside the attention kernels (where the shape allows); "
+                         "explicit: exchange kernels between the attention calls")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sl", type=int, default=4096, help="oracle sample length for cpu_baseline")
@@ -458,8 +518,11 @@ def main():
         offs = doc_offsets_for(w)
         fl_fwd = attn_flops(w, offs=offs)
         fl_bwd = 2.5 * fl_fwd if w.backward else 0.0
-        fwd_tf = fl_fwd / (r["fwd_ms"] * 1e-3) / 1e12
-        bwd_tf = fl_bwd / (r["bwd_ms"] * 1e-3) / 1e12 if w.backward else None
+        km = {n: k["ms_per_step"] for n, k in r["kernels"].items()}
+        attn_fwd_ms = km["attn_fwd"]
+        attn_bwd_ms = sum(km.get(n, 0.0) for n in ("bwd_prep", "bwd_dkdv", "bwd_dq"))
+        fwd_tf = fl_fwd / (attn_fwd_ms * 1e-3) / 1e12
+        bwd_tf = fl_bwd / (attn_bwd_ms * 1e-3) / 1e12 if w.backward else None
         x_bytes = exchange_bytes(w, w.hc) + 2 * exchange_bytes(w, w.hkv)
         s2h_gbs = x_bytes / (r["s2h_qkv_ms"] * 1e-3) / 1e9
         h2s_gbs = exchange_bytes(w, w.hc) / (r["h2s_o_ms"] * 1e-3) / 1e9
@@ -475,8 +538,9 @@ def main():
                                        {"gbs": rate / 1e9, "frac_hbm": rate / 1e9 / peaks["hbm_gbs"]}))
             if name == "bwd_dq":   # S and dP are issued again here: 3 GEMMs run, 1 is its own
                 per_kernel[name]["issued_tflops"] = 3 * rate / 1e12
-        # the dominant kernel: the largest share of the timed device time
-        top = max(r["kernels"], key=lambda n: r["kernels"][n]["total_ms"])
+        # the dominant kernel: the largest share of the timed step's device time
+        top = max((n for n in r["kernels"] if "region" not in r["kernels"][n]),
+                  key=lambda n: r["kernels"][n]["total_ms"])
         cname, bound, units, unit = work[top]
         k = r["kernels"][top]
         avg_ms = k["total_ms"] / k["launches"]
@@ -512,15 +576,24 @@ def main():
                 "gpu_launches": r["launches"],
                 "kernels": per_kernel,
                 "clocks": r["clocks"],
-                "attention": {"fwd_ms": r["fwd_ms"], "fwd_tflops": fwd_tf, "fwd_frac_sustained": fwd_tf / sustained,
-                              "bwd_ms": r["bwd_ms"], "bwd_tflops": bwd_tf,
+                "path": r["path"],
+                "attention": {"fwd_ms": attn_fwd_ms, "fwd_tflops": fwd_tf, "fwd_frac_sustained": fwd_tf / sustained,
+                              "bwd_ms": attn_bwd_ms, "bwd_tflops": bwd_tf,
                               "bwd_frac_sustained": (bwd_tf / sustained) if bwd_tf else None,
-                              "fwd_tflop": fl_fwd / 1e12, "bwd_tflop": fl_bwd / 1e12},
+                              "fwd_tflop": fl_fwd / 1e12, "bwd_tflop": fl_bwd / 1e12,
+                              "kernel_times": "per-kernel CUDA events: forward kernel; backward prep + dK/dV + dQ",
+                              "layer_fwd_ms": r["fwd_ms"], "layer_bwd_ms": r["bwd_ms"],
+                              "layer_times": "CUDA events around the layer's forward and backward calls "
+                                             "(exchanges included)"},
                 "exchange": {"s2h_qkv_ms": r["s2h_qkv_ms"], "s2h_qkv_gbs": s2h_gbs,
                              "s2h_qkv_frac_hbm": s2h_gbs / peaks["hbm_gbs"],
                              "h2s_o_ms": r["h2s_o_ms"], "h2s_o_gbs": h2s_gbs,
                              "h2s_o_frac_hbm": h2s_gbs / peaks["hbm_gbs"],
                              "bytes_rule": "read + write of the whole tensor per exchange",
+                             "timed": ("the explicit exchange kernels in a loop of their own; the fused step runs "
+                                       "none (the attention kernels read and write the sequence shards)"
+                                       if r["path"] == "fused" else "the explicit exchange kernels, in a loop of "
+                                       "their own"),
                              "hbm_peak_gbs": peaks["hbm_gbs"], "hbm_peak_source": src},
                 "context": "pages' figure (not a target): ALST trains a 500K-token sequence for Llama-8B on one H100"}
         print(json.dumps(line), flush=True)

@@ -195,6 +195,60 @@ int ulysses_attn_bwd(ulysses_t h, const void* const* q, const void* const* k,
                      void* workspace, void* stream);
 
 /*
+ * ulysses_layer_fwd — the whole forward of the layer in one call: the
+ * seq->head exchange of Q, K and V, the local attention of ulysses_attn_fwd,
+ * and the head->seq exchange of O. HF blog algorithm steps 3 to 5. The
+ * DeepSpeed-Ulysses blog, section "DeepSpeed-Ulysses的核心设计", places local
+ * attention between the two all-to-alls.
+ *
+ * On one GPU the exchange is a permutation of addresses. Here it is fused
+ * into the attention kernel: its TMA loads read each tile straight from the
+ * sequence shard that holds those tokens, and its epilogue stores O straight
+ * into the sequence shard of its rows. No head-shard copy is made, and no
+ * exchange kernel runs. The results are bit-identical to ulysses_seq_to_head +
+ * ulysses_attn_fwd + ulysses_head_to_seq.
+ *
+ *   q, o     P pointers, each [sl/P][bs][hc][hs]  (sequence shards)
+ *   k, v     P pointers, each [sl/P][bs][hkv][hs] (sequence shards)
+ *   lse      P pointers, each fp32 [bs][hc/P][sl] (output, head layout as in
+ *            ulysses_attn_fwd: rank r's heads [r*hc/P, (r+1)*hc/P))
+ * Returns ULYSSES_ERR_UNSUPPORTED, and enqueues nothing, unless
+ * ulysses_fused_supported(h) is ULYSSES_OK. The explicit three-call path
+ * covers every other shape.
+ */
+int ulysses_layer_fwd(ulysses_t h, const void* const* q, const void* const* k, const void* const* v,
+                      void* const* o, float* const* lse, void* stream);
+
+/*
+ * ulysses_layer_bwd — the whole backward of the layer in one call: dO
+ * seq->head, ulysses_attn_bwd, and dQ, dK, dV head->seq, with both exchanges
+ * fused into the kernels' TMA addressing as in ulysses_layer_fwd.
+ *
+ *   q, o, dO, dq   P pointers, each [sl/P][bs][hc][hs]  (sequence shards)
+ *   k, v, dk, dv   P pointers, each [sl/P][bs][hkv][hs] (sequence shards)
+ *   lse            the forward's fp32 [bs][hc/P][sl] per rank
+ *   workspace      ulysses_workspace_size bytes, as for ulysses_attn_bwd
+ * Bit-identical to the explicit path. ULYSSES_ERR_UNSUPPORTED (nothing
+ * enqueued) unless ulysses_fused_supported(h) is ULYSSES_OK.
+ */
+int ulysses_layer_bwd(ulysses_t h, const void* const* q, const void* const* k, const void* const* v,
+                      const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,
+                      void* const* dk, void* const* dv, void* workspace, void* stream);
+
+/*
+ * ulysses_fused_supported — ULYSSES_OK if ulysses_layer_fwd/_bwd accept this
+ * handle, else ULYSSES_ERR_UNSUPPORTED. They need all of:
+ *   - dtype ULYSSES_BF16 and hs = 128 (the tensor-core kernels);
+ *   - P <= 8 (a launch holds one TMA tensor map per shard and operand);
+ *   - sl/P a multiple of 128, so that no 128-row tile spans two shards;
+ *   - hkv % P == 0 (replicated kv heads need the replica sum of
+ *     ulysses_head_to_seq).
+ * An empty layer (sl = 0 or bs = 0) reports what its shape would allow; the
+ * layer calls are no-ops for it either way. Host only.
+ */
+int ulysses_fused_supported(ulysses_t h);
+
+/*
  * ulysses_get_status — read and clear the handle's device status word.
  * Synchronises the device. Returns ULYSSES_OK, ULYSSES_ERR_TIMEOUT if a
  * bounded device-side wait ran out since the last call (the kernel then

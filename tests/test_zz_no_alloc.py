@@ -32,7 +32,7 @@ def u():
 
 def _forward(u, sl, hc, hkv, P, seed, offs=None):
     x = random_inputs(sl, 1, hc, hkv, 128, torch.bfloat16, seed)
-    L = u.UlyssesLayer(sl, 1, hc, hkv, 128, P, True, offs, torch.bfloat16)
+    L = u.UlyssesLayer(sl, 1, hc, hkv, 128, P, True, offs, torch.bfloat16, fused=False)
     cu = lambda t: [s.cuda() for s in split_shards(t, P)]  # noqa: E731
     o = L.new_seq_shards(hc)
     L.forward(cu(x["q"]), cu(x["k"]), cu(x["v"]), o)

@@ -13,5 +13,6 @@ from ._binding import (  # noqa: F401
     ulysses_create, ulysses_destroy, ulysses_get_status, ulysses_head_to_seq, ulysses_launch_count, ulysses_seq_to_head,
     ulysses_strerror, ulysses_workspace_size, ulysses_set_wait_limit, ulysses_inject_fault,
     ulysses_timing_enable, ulysses_timing_read, ULYSSES_KERNEL_COUNT, KERNEL_NAMES,
+    ulysses_fused_supported, ulysses_layer_fwd, ulysses_layer_bwd,
 )
 from .layer import UlyssesLayer  # noqa: F401

@@ -69,6 +69,12 @@ lib.ulysses_attn_fwd.argtypes = [_vp, _pp, _pp, _pp, _pp, _pp, _vp]
 lib.ulysses_attn_fwd.restype = ctypes.c_int
 lib.ulysses_attn_bwd.argtypes = [_vp] + [_pp] * 9 + [_vp, _vp]
 lib.ulysses_attn_bwd.restype = ctypes.c_int
+lib.ulysses_layer_fwd.argtypes = [_vp, _pp, _pp, _pp, _pp, _pp, _vp]
+lib.ulysses_layer_fwd.restype = ctypes.c_int
+lib.ulysses_layer_bwd.argtypes = [_vp] + [_pp] * 9 + [_vp, _vp]
+lib.ulysses_layer_bwd.restype = ctypes.c_int
+lib.ulysses_fused_supported.argtypes = [_vp]
+lib.ulysses_fused_supported.restype = ctypes.c_int
 lib.ulysses_get_status.argtypes = [_vp]
 lib.ulysses_get_status.restype = ctypes.c_int
 lib.ulysses_attn_bwd_noalloc.argtypes = [_vp] + [_pp] * 9 + [_vp]
@@ -220,18 +226,54 @@ def ulysses_attn_bwd(h: UlyssesHandle, q, k, v, o, do, lse, dq, dk, dv, workspac
     dt = h.torch_dtype
     nq = h.sl * h.bs * h.Hq * h.hs
     nk = h.sl * h.bs * h.Hk * h.hs
-    if isinstance(workspace, torch.Tensor):
-        need = ulysses_workspace_size(h)
-        if workspace.device.type != "cuda" or workspace.numel() * workspace.element_size() < need:
-            raise ValueError(f"workspace must be a CUDA buffer of at least {need} bytes")
-        ws = workspace.data_ptr()
-    else:
-        ws = int(workspace)
+    ws = _workspace_ptr(h, workspace)
     args = [_ptrs(h, q, nq, dt, "q"), _ptrs(h, k, nk, dt, "k"), _ptrs(h, v, nk, dt, "v"),
             _ptrs(h, o, nq, dt, "o"), _ptrs(h, do, nq, dt, "do"),
             _ptrs(h, lse, h.bs * h.Hq * h.sl, torch.float32, "lse"),
             _ptrs(h, dq, nq, dt, "dq"), _ptrs(h, dk, nk, dt, "dk"), _ptrs(h, dv, nk, dt, "dv")]
     _check(lib.ulysses_attn_bwd(h.ptr, *args, ws, _stream(stream)), "ulysses_attn_bwd")
+
+
+def _workspace_ptr(h: UlyssesHandle, workspace) -> int:
+    if isinstance(workspace, torch.Tensor):
+        need = ulysses_workspace_size(h)
+        if workspace.device.type != "cuda" or workspace.numel() * workspace.element_size() < need:
+            raise ValueError(f"workspace must be a CUDA buffer of at least {need} bytes")
+        return workspace.data_ptr()
+    return int(workspace)
+
+
+def ulysses_fused_supported(h: UlyssesHandle) -> bool:
+    """True when ulysses_layer_fwd / ulysses_layer_bwd accept this handle."""
+    st = int(lib.ulysses_fused_supported(h.ptr))
+    if st not in (ULYSSES_OK, ULYSSES_ERR_UNSUPPORTED):
+        _check(st, "ulysses_fused_supported")
+    return st == ULYSSES_OK
+
+
+def ulysses_layer_fwd(h: UlyssesHandle, q, k, v, o, lse, stream=None):
+    """Forward on sequence shards; both exchanges fused into the attention kernel."""
+    dt = h.torch_dtype
+    n = h.sl // h.P
+    nq = n * h.bs * h.hc * h.hs
+    nk = n * h.bs * h.hkv * h.hs
+    args = [_ptrs(h, q, nq, dt, "q"), _ptrs(h, k, nk, dt, "k"), _ptrs(h, v, nk, dt, "v"),
+            _ptrs(h, o, nq, dt, "o"), _ptrs(h, lse, h.bs * h.Hq * h.sl, torch.float32, "lse")]
+    _check(lib.ulysses_layer_fwd(h.ptr, *args, _stream(stream)), "ulysses_layer_fwd")
+
+
+def ulysses_layer_bwd(h: UlyssesHandle, q, k, v, o, do, lse, dq, dk, dv, workspace, stream=None):
+    """Backward on sequence shards; both exchanges fused into the attention kernels."""
+    dt = h.torch_dtype
+    n = h.sl // h.P
+    nq = n * h.bs * h.hc * h.hs
+    nk = n * h.bs * h.hkv * h.hs
+    ws = _workspace_ptr(h, workspace)
+    args = [_ptrs(h, q, nq, dt, "q"), _ptrs(h, k, nk, dt, "k"), _ptrs(h, v, nk, dt, "v"),
+            _ptrs(h, o, nq, dt, "o"), _ptrs(h, do, nq, dt, "do"),
+            _ptrs(h, lse, h.bs * h.Hq * h.sl, torch.float32, "lse"),
+            _ptrs(h, dq, nq, dt, "dq"), _ptrs(h, dk, nk, dt, "dk"), _ptrs(h, dv, nk, dt, "dv")]
+    _check(lib.ulysses_layer_bwd(h.ptr, *args, ws, _stream(stream)), "ulysses_layer_bwd")
 
 
 def ulysses_get_status(h: UlyssesHandle) -> int:

@@ -58,6 +58,10 @@ static_assert(2 * 128 * kRegsCompute + 128 * kRegsOther <= kThreads * kRegsLaunc
 constexpr uint32_t kTile = 128 * 128 * 2;  // a 128x128 bf16 tile: 32 KB
 constexpr uint32_t kHalf = kTile / 2;      // 16 KB
 
+static_assert(kMaxFusedP <= kRanksPerLaunch, "a fused launch holds one tensor map per sequence shard");
+
+// Tensor maps ta..th: one per rank of the launch (head shards), or one per
+// sequence shard (fused; see locate_tile). tr and rows are per rank.
 struct PairParams {
   CUtensorMap ta[kRanksPerLaunch];   // dkdv: K 64x128     dq: Q 64x128
   CUtensorMap tb[kRanksPerLaunch];   // dkdv: V 64x128     dq: dO 64x128
@@ -75,6 +79,8 @@ struct PairParams {
   unsigned* status;
   long long timeout;
   int ndoc, sl, bs, Hq, Hk, group, nranks, causal;
+  int fused;                         // operands are sequence shards of n tokens (nranks = P)
+  int n;
   int pitch;                         // floats per row of a row plane (sl rounded up to 4)
   float scale, scale_log2;
 };
@@ -124,6 +130,7 @@ enum {
   B_REMPTY = B_RFULL + NR,   // NR: rows read by this CTA's compute warps (8 warps)
   B_COUNT = B_REMPTY + NR
 };
+static_assert(8 * B_COUNT + 16 + 12 <= 256, "barriers, TMEM slot and key location fit the barrier area");
 }  // namespace dkdv
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -137,6 +144,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * B_COUNT);
+  // Where this CTA's keys live, found once at set-up and read back by the
+  // producer and the epilogue (computed in both, it would stay live in
+  // every warp role).
+  int* kv_loc = reinterpret_cast<int*>(smem + kOffBar + 8 * B_COUNT + 16);
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   float* rows = reinterpret_cast<float*>(smem + kOffRow);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -167,6 +178,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     fence_mbar_init();
   }
+  if (warp == 8 && lane == 0) {
+    const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hk, hk, kv0);
+    kv_loc[0] = l.map;
+    kv_loc[1] = l.head;
+    kv_loc[2] = l.row;
+  }
   if (warp == 9) {
     tmem_alloc2(smem_u32(tmem_slot), 512);
     tmem_relinquish2();
@@ -183,15 +200,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 8) {
       // --------------------------------------------------------- TMA producer
       bool ok = true;
-      int last[NQ], last_h[NQ], last_r[NR];
-      for (int i = 0; i < NQ; ++i) last[i] = last_h[i] = -1;
-      for (int i = 0; i < NR; ++i) last_r[i] = -1;
+      // Loads issued so far per ring (rows, query parts, head parts): the
+      // last phase armed on slot i of a ring of R slots after c issues is
+      // (c - 1 - i) / R, if c > i.
+      int n_r = 0, n_q = 0, n_h = 0;
       if (lane == 0) {
+        const TileLoc l = {kv_loc[0], kv_loc[1], kv_loc[2]};
         mbar_expect_tx(bar(B_KV), 2 * kTile);
-        tma_load_4d(sb + kOffK, &p.ta[rl], bar(B_KV), 0, hk, b, kv0);
-        tma_load_4d(sb + kOffK + kHalf, &p.ta[rl], bar(B_KV), 64, hk, b, kv0);
-        tma_load_4d(sb + kOffV, &p.tb[rl], bar(B_KV), 0, hk, b, kv0);
-        tma_load_4d(sb + kOffV + kHalf, &p.tb[rl], bar(B_KV), 64, hk, b, kv0);
+        tma_load_4d(sb + kOffK, &p.ta[l.map], bar(B_KV), 0, l.head, b, l.row);
+        tma_load_4d(sb + kOffK + kHalf, &p.ta[l.map], bar(B_KV), 64, l.head, b, l.row);
+        tma_load_4d(sb + kOffV, &p.tb[l.map], bar(B_KV), 0, l.head, b, l.row);
+        tma_load_4d(sb + kOffV + kHalf, &p.tb[l.map], bar(B_KV), 64, l.head, b, l.row);
       }
       for (int it = 0; it < n_it; ++it) {
         const int st = it % NQ, u = it / NQ;
@@ -209,38 +228,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_expect_tx(bar(B_RFULL + rsl), 1024);
           tma_load_3d(sb + kOffRow + rsl * 1024, &p.tr[rl], bar(B_RFULL + rsl), q0, b * p.Hq + hq, 0);
         }
-        last_r[rsl] = it / NR;
+        n_r = it + 1;
+        // Both parts come from the same shard: the tile's rows are in one shard.
+        const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hq, hq, q0);
         // query-half part: Q and dO rows [q0 + 64c, +64) (B of S^T, dP^T: N = queries)
         ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QEMPTY + st), (u & 1) ^ 1, lim));
         if (!ok) break;
         if (lane == 0) {
-          const int qh = q0 + 64 * (int)crank;
+          const int qh = l.row + 64 * (int)crank;
           mbar_expect_tx(bar(B_QFULL + st), 2 * kHalf);
-          tma_load_4d(sq, &p.tc[rl], bar(B_QFULL + st), 0, hq, b, qh);
-          tma_load_4d(sq + kHalf / 2, &p.tc[rl], bar(B_QFULL + st), 64, hq, b, qh);
-          tma_load_4d(sq + kHalf, &p.td[rl], bar(B_QFULL + st), 0, hq, b, qh);
-          tma_load_4d(sq + kHalf + kHalf / 2, &p.td[rl], bar(B_QFULL + st), 64, hq, b, qh);
+          tma_load_4d(sq, &p.tc[l.map], bar(B_QFULL + st), 0, l.head, b, qh);
+          tma_load_4d(sq + kHalf / 2, &p.tc[l.map], bar(B_QFULL + st), 64, l.head, b, qh);
+          tma_load_4d(sq + kHalf, &p.td[l.map], bar(B_QFULL + st), 0, l.head, b, qh);
+          tma_load_4d(sq + kHalf + kHalf / 2, &p.td[l.map], bar(B_QFULL + st), 64, l.head, b, qh);
         }
-        last[st] = u;
+        n_q = it + 1;
         // head-half part: Q and dO columns [64c, 64c+64) of all 128 rows (B of dK, dV)
         ok = __all_sync(0xffffffffu, mbar_wait(bar(B_HEMPTY + st), (u & 1) ^ 1, lim));
         if (!ok) break;
         if (lane == 0) {
           mbar_expect_tx(bar(B_HFULL + st), 2 * kHalf);
-          tma_load_4d(sq + 2 * kHalf, &p.te[rl], bar(B_HFULL + st), 64 * (int)crank, hq, b, q0);
-          tma_load_4d(sq + 3 * kHalf, &p.tf[rl], bar(B_HFULL + st), 64 * (int)crank, hq, b, q0);
+          tma_load_4d(sq + 2 * kHalf, &p.te[l.map], bar(B_HFULL + st), 64 * (int)crank, l.head, b, l.row);
+          tma_load_4d(sq + 3 * kHalf, &p.tf[l.map], bar(B_HFULL + st), 64 * (int)crank, l.head, b, l.row);
         }
-        last_h[st] = u;
+        n_h = it + 1;
       }
       if (lane == 0) {
         if (!ok) pair_status(p);
         mbar_wait(bar(B_KV), 0, lim);
         for (int i = 0; i < NQ; ++i) {
-          if (last[i] >= 0) mbar_wait(bar(B_QFULL + i), last[i] & 1, lim);
-          if (last_h[i] >= 0) mbar_wait(bar(B_HFULL + i), last_h[i] & 1, lim);
+          if (n_q > i) mbar_wait(bar(B_QFULL + i), ((n_q - 1 - i) / NQ) & 1, lim);
+          if (n_h > i) mbar_wait(bar(B_HFULL + i), ((n_h - 1 - i) / NQ) & 1, lim);
         }
         for (int i = 0; i < NR; ++i)
-          if (last_r[i] >= 0) mbar_wait(bar(B_RFULL + i), last_r[i] & 1, lim);
+          if (n_r > i) mbar_wait(bar(B_RFULL + i), ((n_r - 1 - i) / NR) & 1, lim);
       }
       __syncwarp();
     } else if (warp == 9 && crank == 0) {
@@ -450,10 +471,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       warp_arrive_local(bar(B_EPI));
       if (threadIdx.x == 0) {
         if (mbar_wait(bar(B_EPI), 0, lim)) {
-          tma_store_4d(&p.th[rl], sb + kOffV, 0, hk, b, kv0);
-          tma_store_4d(&p.th[rl], sb + kOffV + kHalf, 64, hk, b, kv0);
-          tma_store_4d(&p.tg[rl], sb + kOffK, 0, hk, b, kv0);
-          tma_store_4d(&p.tg[rl], sb + kOffK + kHalf, 64, hk, b, kv0);
+          const TileLoc l = {kv_loc[0], kv_loc[1], kv_loc[2]};
+          tma_store_4d(&p.th[l.map], sb + kOffV, 0, l.head, b, l.row);
+          tma_store_4d(&p.th[l.map], sb + kOffV + kHalf, 64, l.head, b, l.row);
+          tma_store_4d(&p.tg[l.map], sb + kOffK, 0, l.head, b, l.row);
+          tma_store_4d(&p.tg[l.map], sb + kOffK + kHalf, 64, l.head, b, l.row);
           bulk_commit();
           bulk_wait_all();
         } else {
@@ -560,25 +582,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool ok = true;
         int last[NK];
         for (int i = 0; i < NK; ++i) last[i] = -1;
+        const TileLoc lq = locate_tile(p.fused, p.n, p.nranks, rl, p.Hq, hq, q0);
         mbar_expect_tx(bar(B_QO), 2 * kTile);
-        tma_load_4d(sb + kOffQ, &p.ta[rl], bar(B_QO), 0, hq, b, q0);
-        tma_load_4d(sb + kOffQ + kHalf, &p.ta[rl], bar(B_QO), 64, hq, b, q0);
-        tma_load_4d(sb + kOffDO, &p.tb[rl], bar(B_QO), 0, hq, b, q0);
-        tma_load_4d(sb + kOffDO + kHalf, &p.tb[rl], bar(B_QO), 64, hq, b, q0);
+        tma_load_4d(sb + kOffQ, &p.ta[lq.map], bar(B_QO), 0, lq.head, b, lq.row);
+        tma_load_4d(sb + kOffQ + kHalf, &p.ta[lq.map], bar(B_QO), 64, lq.head, b, lq.row);
+        tma_load_4d(sb + kOffDO, &p.tb[lq.map], bar(B_QO), 0, lq.head, b, lq.row);
+        tma_load_4d(sb + kOffDO + kHalf, &p.tb[lq.map], bar(B_QO), 64, lq.head, b, lq.row);
         for (int jj = 0; jj < n_kv; ++jj) {
           const int st = jj % NK, u = jj / NK;
           const int k0 = (kr.x + jj) * 128;
-          const int kh = k0 + 64 * (int)crank;
           if (!mbar_wait(bar(B_KEMPTY + st), (u & 1) ^ 1, lim)) { ok = false; break; }
           const uint32_t sk = sb + kOffStage + st * kStage;
           mbar_expect_tx(bar(B_KFULL + st), 3 * kHalf);
-          // key half of K and V (B of S, dP: N = keys)
-          tma_load_4d(sk, &p.tc[rl], bar(B_KFULL + st), 0, hk, b, kh);
-          tma_load_4d(sk + kHalf / 2, &p.tc[rl], bar(B_KFULL + st), 64, hk, b, kh);
-          tma_load_4d(sk + kHalf, &p.td[rl], bar(B_KFULL + st), 0, hk, b, kh);
-          tma_load_4d(sk + kHalf + kHalf / 2, &p.td[rl], bar(B_KFULL + st), 64, hk, b, kh);
+          // key half of K and V (B of S, dP: N = keys); the tile's keys are in one shard
+          const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hk, hk, k0);
+          const int rn = l.row + 64 * (int)crank;
+          tma_load_4d(sk, &p.tc[l.map], bar(B_KFULL + st), 0, l.head, b, rn);
+          tma_load_4d(sk + kHalf / 2, &p.tc[l.map], bar(B_KFULL + st), 64, l.head, b, rn);
+          tma_load_4d(sk + kHalf, &p.td[l.map], bar(B_KFULL + st), 0, l.head, b, rn);
+          tma_load_4d(sk + kHalf + kHalf / 2, &p.td[l.map], bar(B_KFULL + st), 64, l.head, b, rn);
           // head-dimension half of K (B of dQ: N = head dimension)
-          tma_load_4d(sk + 2 * kHalf, &p.te[rl], bar(B_KFULL + st), 64 * (int)crank, hk, b, k0);
+          tma_load_4d(sk + 2 * kHalf, &p.te[l.map], bar(B_KFULL + st), 64 * (int)crank, l.head, b, l.row);
           last[st] = u;
         }
         if (!ok) pair_status(p);
@@ -742,8 +766,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       warp_arrive_local(bar(B_EPI));
       if (threadIdx.x == 0) {
         if (mbar_wait(bar(B_EPI), 0, lim)) {
-          tma_store_4d(&p.tf[rl], sb + kOffQ, 0, hq, b, q0);
-          tma_store_4d(&p.tf[rl], sb + kOffQ + kHalf, 64, hq, b, q0);
+          const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hq, hq, q0);
+          tma_store_4d(&p.tf[l.map], sb + kOffQ, 0, l.head, b, l.row);
+          tma_store_4d(&p.tf[l.map], sb + kOffQ + kHalf, 64, l.head, b, l.row);
           bulk_commit();
           bulk_wait_all();
         } else {
@@ -766,13 +791,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // The row planes of the backward, for every (rank, batch, head, row):
 // -LSE * log2(e) (plane 0) and D = rowsum(dO * O) (plane 1), each
-// [bs][Hq][pitch] fp32. 16 lanes per row.
+// [bs][Hq][pitch] fp32. 16 lanes per row. O and dO are head shards, or
+// sequence shards when fused (row t of rank r's head hq is then token
+// t - s*n of shard s = t / n, head r*Hq + hq).
 struct PrepParams {
   const __nv_bfloat16* o[ULYSSES_MAX_P];
   const __nv_bfloat16* dO[ULYSSES_MAX_P];
   const float* lse[ULYSSES_MAX_P];
   float* rows[ULYSSES_MAX_P];
   int P, sl, bs, Hq, pitch;
+  int fused, n;
   long long rows_per_rank;  // sl * bs * Hq
 };
 
@@ -791,8 +819,17 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constan
     const long long rr = row - (long long)r * a.rows_per_rank;  // (t, b, hq)
     float acc = 0.f;
     if (active) {
-      const uint4 ov = *reinterpret_cast<const uint4*>(a.o[r] + rr * 128 + part * 8);
-      const uint4 dv = *reinterpret_cast<const uint4*>(a.dO[r] + rr * 128 + part * 8);
+      int src = r;
+      long long at = rr;  // row index (t, b, hq) within the source buffer
+      if (a.fused) {
+        const int hq = (int)(rr % a.Hq);
+        const long long tb = rr / a.Hq;
+        const long long t = tb / a.bs;
+        src = (int)(t / a.n);
+        at = ((tb - (long long)src * a.n * a.bs) * a.P + r) * a.Hq + hq;
+      }
+      const uint4 ov = *reinterpret_cast<const uint4*>(a.o[src] + at * 128 + part * 8);
+      const uint4 dv = *reinterpret_cast<const uint4*>(a.dO[src] + at * 128 + part * 8);
       const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
       const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
 #pragma unroll
@@ -865,7 +902,8 @@ static int grid_cap(long long work) {
 
 int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* const* k, const void* const* v,
                           const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,
-                          void* const* dk, void* const* dv, void* workspace, cudaStream_t stream) {
+                          void* const* dk, void* const* dv, void* workspace, cudaStream_t stream, bool fused) {
+  if (fused && !fused_supported(L)) return ULYSSES_ERR_UNSUPPORTED;
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dkdv::kSmem) !=
@@ -896,6 +934,8 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
     a.bs = (int)L.bs;
     a.Hq = L.Hq;
     a.pitch = (int)pitch;
+    a.fused = fused ? 1 : 0;
+    a.n = (int)L.n();
     a.rows_per_rank = (long long)L.sl * L.bs * L.Hq;
     Timed t(L.timing, ULYSSES_KERNEL_BWD_PREP, stream);
     attn_bwd_prep_kernel<<<grid_cap(a.rows_per_rank * L.P * 16), 256, 0, stream>>>(a);
@@ -914,9 +954,15 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
   prm.group = L.Hq / L.Hk;
   prm.causal = L.causal;
   prm.pitch = (int)pitch;
+  prm.fused = fused ? 1 : 0;
+  prm.n = (int)L.n();
   prm.scale = (float)(1.0 / sqrt((double)L.hs));
   prm.scale_log2 = (float)(1.4426950408889634 / sqrt((double)L.hs));
   const int n_pair = (int)((L.sl + 255) / 256);
+  // Fused: one launch covers all P ranks, and map i is sequence shard i,
+  // [n][bs][H][hs] with every head. Otherwise map i is head shard r0 + i.
+  const int64_t R = fused ? L.n() : L.sl;
+  const int mq = fused ? L.hc : L.Hq, mk = fused ? L.hkv : L.Hk;
   for (int pass = 0; pass < 2; ++pass) {  // 2. dK, dV   3. dQ
     prm.range = pass == 0 ? L.d_kvp_range : L.d_qp_range;
     prm.order = pass == 0 ? L.d_kvp_order : L.d_qp_order;
@@ -927,23 +973,23 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
         const int r = r0 + i;
         bool ok;
         if (pass == 0)
-          ok = make_tmap_bf16_4d(&prm.ta[i], k[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
-               make_tmap_bf16_4d(&prm.tb[i], v[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
-               make_tmap_bf16_4d(&prm.tc[i], q[r], 128, L.Hq, L.bs, L.sl, 64, 64) &&
-               make_tmap_bf16_4d(&prm.td[i], dO[r], 128, L.Hq, L.bs, L.sl, 64, 64) &&
-               make_tmap_bf16_4d(&prm.te[i], q[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
-               make_tmap_bf16_4d(&prm.tf[i], dO[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
-               make_tmap_bf16_4d(&prm.tg[i], dk[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
-               make_tmap_bf16_4d(&prm.th[i], dv[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
+          ok = make_tmap_bf16_4d(&prm.ta[i], k[r], 128, mk, L.bs, R, 64, 128) &&
+               make_tmap_bf16_4d(&prm.tb[i], v[r], 128, mk, L.bs, R, 64, 128) &&
+               make_tmap_bf16_4d(&prm.tc[i], q[r], 128, mq, L.bs, R, 64, 64) &&
+               make_tmap_bf16_4d(&prm.td[i], dO[r], 128, mq, L.bs, R, 64, 64) &&
+               make_tmap_bf16_4d(&prm.te[i], q[r], 128, mq, L.bs, R, 64, 128) &&
+               make_tmap_bf16_4d(&prm.tf[i], dO[r], 128, mq, L.bs, R, 64, 128) &&
+               make_tmap_bf16_4d(&prm.tg[i], dk[r], 128, mk, L.bs, R, 64, 128) &&
+               make_tmap_bf16_4d(&prm.th[i], dv[r], 128, mk, L.bs, R, 64, 128) &&
                make_tmap_f32_rows(&prm.tr[i], ws + per_rank * r, (uint64_t)L.sl, (uint64_t)nrows,
                                   (uint64_t)pitch);
         else
-          ok = make_tmap_bf16_4d(&prm.ta[i], q[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
-               make_tmap_bf16_4d(&prm.tb[i], dO[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
-               make_tmap_bf16_4d(&prm.tc[i], k[r], 128, L.Hk, L.bs, L.sl, 64, 64) &&
-               make_tmap_bf16_4d(&prm.td[i], v[r], 128, L.Hk, L.bs, L.sl, 64, 64) &&
-               make_tmap_bf16_4d(&prm.te[i], k[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
-               make_tmap_bf16_4d(&prm.tf[i], dq[r], 128, L.Hq, L.bs, L.sl, 64, 128);
+          ok = make_tmap_bf16_4d(&prm.ta[i], q[r], 128, mq, L.bs, R, 64, 128) &&
+               make_tmap_bf16_4d(&prm.tb[i], dO[r], 128, mq, L.bs, R, 64, 128) &&
+               make_tmap_bf16_4d(&prm.tc[i], k[r], 128, mk, L.bs, R, 64, 64) &&
+               make_tmap_bf16_4d(&prm.td[i], v[r], 128, mk, L.bs, R, 64, 64) &&
+               make_tmap_bf16_4d(&prm.te[i], k[r], 128, mk, L.bs, R, 64, 128) &&
+               make_tmap_bf16_4d(&prm.tf[i], dq[r], 128, mq, L.bs, R, 64, 128);
         if (!ok) return ULYSSES_ERR_CUDA;
         prm.rows[i] = ws + per_rank * r;
       }

@@ -70,18 +70,24 @@ constexpr uint32_t kStage = 2 * kHalf;
 constexpr uint32_t kOffBar = kOffStage + NS * kStage;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
 
+static_assert(kMaxFusedP <= kRanksPerLaunch, "a fused launch holds one tensor map per sequence shard");
+
+// Tensor maps: one per rank of the launch (head shards), or one per sequence
+// shard (fused; see locate_tile).
 struct FwdParams {
   CUtensorMap tq[kRanksPerLaunch];   // Q, boxes of 64 columns x 128 rows
   CUtensorMap tk[kRanksPerLaunch];   // K, boxes of 64 columns x 64 rows
   CUtensorMap tv[kRanksPerLaunch];   // V, boxes of 64 columns x 128 rows
   CUtensorMap to[kRanksPerLaunch];   // O (store), boxes of 64 columns x 128 rows
-  float* lse[kRanksPerLaunch];
+  float* lse[kRanksPerLaunch];       // per rank of the launch
   const int2* kv_range;   // per 256-row block: first and last key tile (inclusive)
   const int* m_order;     // row blocks, most key tiles first
   const int32_t* doc_offsets;
   unsigned* status;
   long long timeout;      // clock cycles per wait
   int ndoc, sl, bs, Hq, Hk, group, npairs, nranks, causal;
+  int fused;              // operands are sequence shards of n tokens (nranks = P)
+  int n;
   int skip_kv_loads;      // test hook: the producer issues no K/V loads
   float scale_log2;
 };
@@ -161,8 +167,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_expect_tx(bar(B_QFULL), ntile * kTile);
         for (int t = 0; t < ntile; ++t) {
           const uint32_t dst = sQ0 + t * kTile;
-          tma_load_4d(dst, &p.tq[rl], bar(B_QFULL), 0, hq0 + t, b, q0);
-          tma_load_4d(dst + kHalf, &p.tq[rl], bar(B_QFULL), 64, hq0 + t, b, q0);
+          const TileLoc lq = locate_tile(p.fused, p.n, p.nranks, rl, p.Hq, hq0 + t, q0);
+          tma_load_4d(dst, &p.tq[lq.map], bar(B_QFULL), 0, lq.head, b, lq.row);
+          tma_load_4d(dst + kHalf, &p.tq[lq.map], bar(B_QFULL), 64, lq.head, b, lq.row);
         }
         for (int jj = 0; jj < (p.skip_kv_loads ? 0 : n_kv); ++jj) {
           const int st = jj % NS, u = jj / NS;
@@ -170,11 +177,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar(B_KVEMPTY + st), (u & 1) ^ 1, lim)) { ok = false; break; }
           const uint32_t sk = sb + kOffStage + st * kStage;
           mbar_expect_tx(bar(B_KVFULL + st), kStage);
+          // the tile's 128 keys are in one shard
+          const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hk, hk, k0);
           // K rows [k0 + 64c, +64) (the N half of B for S = Q K^T), K-major in two 64-column boxes
-          tma_load_4d(sk, &p.tk[rl], bar(B_KVFULL + st), 0, hk, b, k0 + 64 * (int)crank);
-          tma_load_4d(sk + kHalf / 2, &p.tk[rl], bar(B_KVFULL + st), 64, hk, b, k0 + 64 * (int)crank);
+          tma_load_4d(sk, &p.tk[l.map], bar(B_KVFULL + st), 0, l.head, b, l.row + 64 * (int)crank);
+          tma_load_4d(sk + kHalf / 2, &p.tk[l.map], bar(B_KVFULL + st), 64, l.head, b, l.row + 64 * (int)crank);
           // V columns [64c, 64c+64) of all 128 key rows (the N half of B for O += P V), MN-major
-          tma_load_4d(sk + kHalf, &p.tv[rl], bar(B_KVFULL + st), 64 * (int)crank, hk, b, k0);
+          tma_load_4d(sk + kHalf, &p.tv[l.map], bar(B_KVFULL + st), 64 * (int)crank, l.head, b, l.row);
           last[st] = u;
         }
         if (!ok) atomicOr(p.status, STATUS_TIMEOUT);
@@ -383,8 +392,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(B_OSTAGE + t));
         if (rq == 0) {
           if (mbar_wait(bar(B_OSTAGE + t), 0, lim)) {
-            tma_store_4d(&p.to[rl], stage, 0, hq, b, q0);
-            tma_store_4d(&p.to[rl], stage + kHalf, 64, hq, b, q0);
+            const TileLoc lo_ = locate_tile(p.fused, p.n, p.nranks, rl, p.Hq, hq, q0);
+            tma_store_4d(&p.to[lo_.map], stage, 0, lo_.head, b, lo_.row);
+            tma_store_4d(&p.to[lo_.map], stage + kHalf, 64, lo_.head, b, lo_.row);
             bulk_commit();
             bulk_wait_all();
           } else {
@@ -411,8 +421,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 bool fwd_sm103_supported(const Layer& L) { return L.dtype == ULYSSES_BF16 && L.hs == 128; }
 
+bool fused_supported(const Layer& L) {
+  return fwd_sm103_supported(L) && L.P <= kMaxFusedP && L.n() % 128 == 0 && L.hkv % L.P == 0;
+}
+
 int launch_attn_fwd_sm103(Layer& L, const void* const* q, const void* const* k, const void* const* v,
-                          void* const* o, float* const* lse, cudaStream_t stream) {
+                          void* const* o, float* const* lse, cudaStream_t stream, bool fused) {
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(attn_fwd_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
@@ -439,15 +453,22 @@ int launch_attn_fwd_sm103(Layer& L, const void* const* q, const void* const* k, 
   prm.skip_kv_loads = L.inject_fault == 1 ? 1 : 0;
   L.inject_fault = 0;
   prm.scale_log2 = (float)(1.4426950408889634 / sqrt((double)L.hs));
+  prm.fused = fused ? 1 : 0;
+  prm.n = (int)L.n();
+  if (fused && !fused_supported(L)) return ULYSSES_ERR_UNSUPPORTED;
+  // Fused: one launch covers all P ranks, and map i is sequence shard i,
+  // [n][bs][H][hs] with every head. Otherwise map i is head shard r0 + i.
+  const int64_t rows = fused ? L.n() : L.sl;
+  const int mq = fused ? L.hc : L.Hq, mk = fused ? L.hkv : L.Hk;
   for (int r0 = 0; r0 < L.P; r0 += kRanksPerLaunch) {
     const int nr = std::min(kRanksPerLaunch, L.P - r0);
     prm.nranks = nr;
     for (int i = 0; i < nr; ++i) {
       const int r = r0 + i;
-      bool ok = make_tmap_bf16_4d(&prm.tq[i], q[r], 128, L.Hq, L.bs, L.sl, 64, 128) &&
-                make_tmap_bf16_4d(&prm.tk[i], k[r], 128, L.Hk, L.bs, L.sl, 64, 64) &&
-                make_tmap_bf16_4d(&prm.tv[i], v[r], 128, L.Hk, L.bs, L.sl, 64, 128) &&
-                make_tmap_bf16_4d(&prm.to[i], o[r], 128, L.Hq, L.bs, L.sl, 64, 128);
+      bool ok = make_tmap_bf16_4d(&prm.tq[i], q[r], 128, mq, L.bs, rows, 64, 128) &&
+                make_tmap_bf16_4d(&prm.tk[i], k[r], 128, mk, L.bs, rows, 64, 64) &&
+                make_tmap_bf16_4d(&prm.tv[i], v[r], 128, mk, L.bs, rows, 64, 128) &&
+                make_tmap_bf16_4d(&prm.to[i], o[r], 128, mq, L.bs, rows, 64, 128);
       if (!ok) return ULYSSES_ERR_CUDA;
       prm.lse[i] = lse[r];
     }

@@ -241,6 +241,47 @@ int ulysses_attn_bwd(ulysses_t h, const void* const* q, const void* const* k,
                                    (cudaStream_t)stream);
 }
 
+int ulysses_fused_supported(ulysses_t h) {
+  const Layer* L = reinterpret_cast<const Layer*>(h);
+  if (!L) return ULYSSES_ERR_INVALID_ARG;
+  return uly::fused_supported(*L) ? ULYSSES_OK : ULYSSES_ERR_UNSUPPORTED;
+}
+
+int ulysses_layer_fwd(ulysses_t h, const void* const* q, const void* const* k, const void* const* v,
+                      void* const* o, float* const* lse, void* stream) {
+  Layer* L = reinterpret_cast<Layer*>(h);
+  if (!L) return ULYSSES_ERR_INVALID_ARG;
+  if (L->empty()) return ULYSSES_OK;
+  if (!uly::fused_supported(*L)) return ULYSSES_ERR_UNSUPPORTED;
+  CHECK_PTRS(q);
+  CHECK_PTRS(k);
+  CHECK_PTRS(v);
+  CHECK_PTRS(o);
+  CHECK_PTRS(lse);
+  return uly::launch_attn_fwd_sm103(*L, q, k, v, o, lse, (cudaStream_t)stream, true);
+}
+
+int ulysses_layer_bwd(ulysses_t h, const void* const* q, const void* const* k, const void* const* v,
+                      const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,
+                      void* const* dk, void* const* dv, void* workspace, void* stream) {
+  const Layer* L = reinterpret_cast<const Layer*>(h);
+  if (!L) return ULYSSES_ERR_INVALID_ARG;
+  if (L->empty()) return ULYSSES_OK;
+  if (!uly::fused_supported(*L)) return ULYSSES_ERR_UNSUPPORTED;
+  CHECK_PTRS(q);
+  CHECK_PTRS(k);
+  CHECK_PTRS(v);
+  CHECK_PTRS(o);
+  CHECK_PTRS(dO);
+  CHECK_PTRS(lse);
+  CHECK_PTRS(dq);
+  CHECK_PTRS(dk);
+  CHECK_PTRS(dv);
+  if (!workspace) return ULYSSES_ERR_INVALID_ARG;
+  if (((uintptr_t)workspace) & 15u) return ULYSSES_ERR_ALIGNMENT;
+  return uly::launch_attn_bwd_sm103(*L, q, k, v, o, dO, lse, dq, dk, dv, workspace, (cudaStream_t)stream, true);
+}
+
 int ulysses_set_wait_limit(ulysses_t h, int64_t cycles) {
   Layer* L = reinterpret_cast<Layer*>(h);
   if (!L || cycles <= 0) return ULYSSES_ERR_INVALID_ARG;

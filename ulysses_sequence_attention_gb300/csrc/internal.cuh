@@ -179,15 +179,23 @@ int launch_attn_bwd_simt(const Layer& L, const void* const* q, const void* const
                          void* const* dv, void* workspace, cudaStream_t s);
 
 bool fwd_sm103_supported(const Layer& L);
+// Whether the tensor-core kernels can read and write sequence shards directly
+// (the exchanges fused into their TMA addressing): the bf16 hs=128 path, at
+// most kMaxFusedP shards (one tensor map per shard and operand in a launch),
+// shards of a whole number of 128-row tiles, and no replicated kv heads.
+constexpr int kMaxFusedP = 8;
+bool fused_supported(const Layer& L);
+// fused: q, k, v, o are sequence shards (else head shards).
 int launch_attn_fwd_sm103(Layer& L, const void* const* q, const void* const* k, const void* const* v,
-                          void* const* o, float* const* lse, cudaStream_t s);
+                          void* const* o, float* const* lse, cudaStream_t s, bool fused = false);
 
 void plan_pair_tiles(const Layer& L, std::vector<int2>& kv_pairs, std::vector<int>& kv_order,
                      std::vector<int2>& q_pairs, std::vector<int>& q_order);
 size_t bwd_sm103_workspace(const Layer& L);
+// fused: q, k, v, o, dO, dq, dk, dv are sequence shards (else head shards).
 int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* const* k, const void* const* v,
                           const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,
-                          void* const* dk, void* const* dv, void* workspace, cudaStream_t s);
+                          void* const* dk, void* const* dv, void* workspace, cudaStream_t s, bool fused = false);
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA; }
 
@@ -209,6 +217,25 @@ __device__ __forceinline__ int doc_of(const int32_t* offs, int ndoc, int t) {
     if (offs[mid] <= t) lo = mid; else hi = mid - 1;
   }
   return lo;
+}
+
+// Where a tile of rows [t, t + 128) of local head h of rank rl lives, for the
+// TMA tensor maps of the attention kernels.
+//  * Head shards (fused == 0): map rl holds rank rl's heads; coordinates are
+//    (head h, row t).
+//  * Sequence shards (fused != 0): the seq->head exchange read through the
+//    tensor maps. Map s covers shard s, tokens [s*n, (s+1)*n) with every
+//    head, so the tile is in map t / n at head rl*H + h and row t - s*n. A
+//    tile never straddles two shards (n is a multiple of 128). A tile that
+//    starts past the sequence (the odd CTA of a last half pair) is placed in
+//    the last shard at a row >= n, where TMA reads zeros and clips stores.
+struct TileLoc {
+  int map, head, row;
+};
+__device__ __forceinline__ TileLoc locate_tile(int fused, int n, int nshards, int rl, int H, int h, int t) {
+  if (!fused) return {rl, h, t};
+  const int s = min(t / n, nshards - 1);
+  return {s, rl * H + h, t - s * n};
 }
 
 template <typename T> __device__ __forceinline__ float to_f32(T x);

@@ -7,9 +7,17 @@ backward:
   forward:  Q, K, V seq->head  ->  attention forward  ->  O head->seq
   backward: dO seq->head  ->  attention backward  ->  dQ, dK, dV head->seq
 
-Every step is one C-ABI call into libulysses.so. This class only owns the
-intermediate head-shard buffers (torch device memory) and enqueues the calls
-on the current stream.
+Two ways to run them, both through the C-ABI of libulysses.so:
+
+* fused (ulysses_layer_fwd / ulysses_layer_bwd): one call per pass. The
+  attention kernels read the sequence shards and write the outputs back into
+  sequence shards through their TMA tensor maps, so no exchange kernel runs
+  and no head-shard copy exists. Used whenever ulysses_fused_supported allows.
+* explicit: one call per step, with head-shard buffers in between. Used for
+  every other shape, or when asked for with fused=False.
+
+Both give bit-identical results. This class only owns the intermediate buffers
+(torch device memory) and enqueues the calls on the current stream.
 """
 from __future__ import annotations
 
@@ -23,30 +31,37 @@ from . import _binding as B
 class UlyssesLayer:
     def __init__(self, sl: int, bs: int, hc: int, hkv: int, hs: int, P: int, causal: bool = True,
                  doc_offsets: Optional[Sequence[int]] = None, dtype=torch.bfloat16,
-                 device: str = "cuda"):
+                 device: str = "cuda", fused: Optional[bool] = None):
+        """fused: None picks the fused path when the shape allows it; True requires it."""
         self.h = B.ulysses_create(sl, bs, hc, hkv, hs, P, causal, doc_offsets, dtype)
         self.sl, self.bs, self.hc, self.hkv, self.hs, self.P = sl, bs, hc, hkv, hs, P
         self.dtype = dtype
         self.device = device
         self.Hq, self.Hk = self.h.Hq, self.h.Hk
+        can = B.ulysses_fused_supported(self.h)
+        if fused and not can:
+            raise B.UlyssesError(B.ULYSSES_ERR_UNSUPPORTED, "UlyssesLayer(fused=True)")
+        self.fused = can if fused is None else bool(fused)
         self._bufs = None
+        self._saved = None
 
     # -- buffers -----------------------------------------------------------
     def _alloc(self, backward: bool):
         P, sl, bs, hs, dt, dev = self.P, self.sl, self.bs, self.hs, self.dtype, self.device
-        n = sl // P
 
         def heads(H):
             return [torch.empty((sl, bs, H, hs), dtype=dt, device=dev) for _ in range(P)]
 
         b = self._bufs or {}
-        if "qh" not in b:
-            b["qh"], b["kh"], b["vh"], b["oh"] = heads(self.Hq), heads(self.Hk), heads(self.Hk), heads(self.Hq)
+        if "lse" not in b:
             b["lse"] = [torch.empty((bs, self.Hq, sl), dtype=torch.float32, device=dev) for _ in range(P)]
-        if backward and "doh" not in b:
-            b["doh"], b["dqh"], b["dkh"], b["dvh"] = heads(self.Hq), heads(self.Hq), heads(self.Hk), heads(self.Hk)
+        if not self.fused and "qh" not in b:
+            b["qh"], b["kh"], b["vh"], b["oh"] = heads(self.Hq), heads(self.Hk), heads(self.Hk), heads(self.Hq)
+        if backward and "ws" not in b:
             nbytes = B.ulysses_workspace_size(self.h)
             b["ws"] = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=dev)
+        if backward and not self.fused and "doh" not in b:
+            b["doh"], b["dqh"], b["dkh"], b["dvh"] = heads(self.Hq), heads(self.Hq), heads(self.Hk), heads(self.Hk)
         self._bufs = b
         return b
 
@@ -57,8 +72,17 @@ class UlyssesLayer:
 
     # -- steps -------------------------------------------------------------
     def forward(self, q_seq, k_seq, v_seq, o_seq, stream=None):
-        """Seq-sharded Q, K, V in, seq-sharded O out (all lists of P tensors)."""
+        """Seq-sharded Q, K, V in, seq-sharded O out (all lists of P tensors).
+
+        The fused path keeps references to q_seq, k_seq, v_seq and o_seq for
+        the backward, as autograd keeps saved tensors: leave them unchanged
+        until backward has been enqueued.
+        """
         b = self._alloc(backward=False)
+        if self.fused:
+            B.ulysses_layer_fwd(self.h, q_seq, k_seq, v_seq, o_seq, b["lse"], stream)
+            self._saved = (q_seq, k_seq, v_seq, o_seq)
+            return o_seq
         B.ulysses_seq_to_head(self.h, self.hc, q_seq, b["qh"], stream)
         B.ulysses_seq_to_head(self.h, self.hkv, k_seq, b["kh"], stream)
         B.ulysses_seq_to_head(self.h, self.hkv, v_seq, b["vh"], stream)
@@ -69,6 +93,12 @@ class UlyssesLayer:
     def backward(self, do_seq, dq_seq, dk_seq, dv_seq, stream=None):
         """Seq-sharded dO in, seq-sharded dQ, dK, dV out. Uses the last forward's state."""
         b = self._alloc(backward=True)
+        if self.fused:
+            if self._saved is None:
+                raise RuntimeError("UlyssesLayer.backward before forward")
+            q, k, v, o = self._saved
+            B.ulysses_layer_bwd(self.h, q, k, v, o, do_seq, b["lse"], dq_seq, dk_seq, dv_seq, b["ws"], stream)
+            return dq_seq, dk_seq, dv_seq
         B.ulysses_seq_to_head(self.h, self.hc, do_seq, b["doh"], stream)
         B.ulysses_attn_bwd(self.h, b["qh"], b["kh"], b["vh"], b["oh"], b["doh"], b["lse"],
                            b["dqh"], b["dkh"], b["dvh"], b["ws"], stream)
