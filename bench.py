@@ -361,40 +361,69 @@ def run_ours(args, w, rank, world):
 
 
 def run_e2e(args, w, L, x, dev, world, barrier):
-    """The same metric through UlyssesLayer with host<->device copies in the timed region."""
+    """The same metric through the public API with host<->device copies in the timed region.
+
+    Fused shapes go through HostSteps (ulysses_host_begin/_step/_end): each
+    step copies its Q/K/V/dO shards in from pinned host memory and its
+    O/dQ/dK/dV shards out, on the library's copy streams, overlapped with the
+    neighbouring steps' kernels. Other shapes run UlyssesLayer with the copies
+    on the compute stream. CUDA events on the compute stream bracket the run;
+    ulysses_host_end makes the closing event wait for every copy.
+    """
+    import ulysses_sequence_attention_gb300 as U
     P = w.P
-    pin = {k: [t.pin_memory() for t in split_shards(v, P)] for k, v in x.items()}
-    dseq = {k: [torch.empty_like(t, device=dev) for t in v] for k, v in pin.items()}
-    o = L.new_seq_shards(w.hc)
-    outs = [o]
-    if w.backward:
-        dq, dk, dv = L.new_seq_shards(w.hc), L.new_seq_shards(w.hkv), L.new_seq_shards(w.hkv)
-        outs += [dq, dk, dv]
-    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in grp] for grp in outs]
-    h2d = sum(t.numel() * t.element_size() for v in pin.values() for t in v)
-    d2h = sum(t.numel() * t.element_size() for grp in outs for t in grp)
     stream = torch.cuda.current_stream(dev)
+    pin = {k: [t.pin_memory() for t in split_shards(v, P)] for k, v in x.items()}
 
-    def step():
-        for k in pin:
-            for src, dst in zip(pin[k], dseq[k]):
-                dst.copy_(src, non_blocking=True)
-        L.forward(dseq["q"], dseq["k"], dseq["v"], o)
+    def host_out():
+        mk = lambda H: [torch.empty((w.sl // P, w.bs, H, w.hs), dtype=w.torch_dtype, pin_memory=True)  # noqa: E731
+                        for _ in range(P)]
+        return {"o": mk(w.hc), "dq": mk(w.hc), "dk": mk(w.hkv), "dv": mk(w.hkv)}
+
+    if L.fused and w.backward:
+        hs = U.HostSteps(L)
+        outs = [host_out(), host_out()]       # one set per device slot
+        h2d, d2h = hs.host_bytes_per_step()
+
+        def run(nsteps):
+            hs.begin(stream)
+            for i in range(nsteps):
+                hs.step(pin, outs[i % 2], stream)
+            hs.end(stream)
+        how = "HostSteps: copies on the library's copy streams, overlapped with neighbouring steps"
+    else:
+        dseq = {k: [torch.empty_like(t, device=dev) for t in v] for k, v in pin.items()}
+        o = L.new_seq_shards(w.hc)
+        outs_dev = [o]
         if w.backward:
-            L.backward(dseq["do"], dq, dk, dv)
-        for grp, hgrp in zip(outs, host_out):
-            for src, dst in zip(grp, hgrp):
-                dst.copy_(src, non_blocking=True)
+            dq, dk, dv = L.new_seq_shards(w.hc), L.new_seq_shards(w.hkv), L.new_seq_shards(w.hkv)
+            outs_dev += [dq, dk, dv]
+        host = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in grp] for grp in outs_dev]
+        h2d = sum(t.numel() * t.element_size() for k, v in pin.items() if w.backward or k != "do" for t in v)
+        d2h = sum(t.numel() * t.element_size() for grp in outs_dev for t in grp)
 
-    for _ in range(args.warmup):
-        step()
+        def run(nsteps):
+            for _ in range(nsteps):
+                for k in pin:
+                    if k == "do" and not w.backward:
+                        continue
+                    for src, dst in zip(pin[k], dseq[k]):
+                        dst.copy_(src, non_blocking=True)
+                L.forward(dseq["q"], dseq["k"], dseq["v"], o)
+                if w.backward:
+                    L.backward(dseq["do"], dq, dk, dv)
+                for grp, hgrp in zip(outs_dev, host):
+                    for src, dst in zip(grp, hgrp):
+                        dst.copy_(src, non_blocking=True)
+        how = "UlyssesLayer with the copies on the compute stream"
+
+    run(args.warmup)
     torch.cuda.synchronize(dev)
     barrier()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(args.steps):
-        step()
+    run(args.steps)
     t1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -404,7 +433,7 @@ def run_e2e(args, w, L, x, dev, world, barrier):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     ms = float(t.item())
     return {"value": w.sl * w.bs * args.steps * world / (ms / 1e3), "unit": "tokens/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps, "how": how}
 
 
 # ---------------------------------------------------------------------------

@@ -249,6 +249,57 @@ int ulysses_layer_bwd(ulysses_t h, const void* const* q, const void* const* k, c
 int ulysses_fused_supported(ulysses_t h);
 
 /*
+ * Host-streaming training steps: ulysses_host_begin, ulysses_host_step,
+ * ulysses_host_end.
+ *
+ * A step is what a training loop feeds the layer. The P sequence shards of Q,
+ * K, V and dO come from HOST memory. The layer runs forward and backward (as
+ * ulysses_layer_fwd + ulysses_layer_bwd), and O, dQ, dK, dV go back to host
+ * memory. In the pages' loop each rank's DataLoader hands it its sequence
+ * shard (ALST guide, section 2.2: the DataLoader adapter and its CPU prefetch
+ * buffer). Here the P shards of a step are P host buffers per tensor.
+ *
+ * The copies run on two copy streams owned by the handle (host->device and
+ * device->host). The kernels run on `stream`. With two slots of device
+ * buffers, used alternately, step i+1's inputs travel while step i computes,
+ * and step i's outputs travel while step i+1 computes. The library orders
+ * every reuse of a slot with events:
+ *   - the copy of inputs into a slot waits for the last compute on that slot;
+ *   - its forward waits for the last copy of outputs out of the slot;
+ *   - the copy of O starts when the forward ends and overlaps the backward.
+ *
+ * ulysses_host_begin(h, stream): the copy streams wait for the work already
+ *   enqueued on `stream`. Call it once before a run of steps.
+ * ulysses_host_end(h, stream): `stream` waits for every copy enqueued so far.
+ *   After it, an event recorded on `stream`, or a synchronisation of `stream`,
+ *   covers all the steps' copies and kernels.
+ * ulysses_host_step(h, slot, host_in, host_out, dev, lse, workspace, stream):
+ *   slot       0 or 1: which set of device buffers `dev` is.
+ *   host_in    4*P HOST pointers: Q shards 0..P-1, then K, V and dO. Use
+ *              pinned memory: pageable memory works, but the copies then stop
+ *              overlapping. Keep them unchanged until ulysses_host_end and a
+ *              synchronisation of `stream`.
+ *   host_out   4*P HOST pointers: O, dQ, dK, dV. Written asynchronously; valid
+ *              after ulysses_host_end and a synchronisation of `stream`.
+ *   dev        8*P DEVICE pointers of this slot: Q, K, V, dO, O, dQ, dK, dV,
+ *              each [sl/P][bs][H][hs] (H = hc or hkv). They must not be used
+ *              elsewhere while the steps run.
+ *   lse        P DEVICE pointers, fp32 [bs][hc/P][sl], shared by both slots.
+ *   workspace  ulysses_workspace_size bytes of DEVICE memory, shared by both slots.
+ *   Every pointer must be non-NULL; device pointers must be 16-byte aligned.
+ *   Shapes must be accepted by ulysses_fused_supported (ULYSSES_ERR_UNSUPPORTED
+ *   otherwise, with nothing enqueued). The first call of a handle creates its two
+ *   copy streams and a few events. It allocates no device memory. Everything
+ *   is enqueued; nothing synchronises.
+ * There is no counterpart of the streams and slots on the pages: they are how
+ * this library keeps the host copies off the critical path.
+ */
+int ulysses_host_begin(ulysses_t h, void* stream);
+int ulysses_host_step(ulysses_t h, int slot, const void* const* host_in, void* const* host_out,
+                      void* const* dev, float* const* lse, void* workspace, void* stream);
+int ulysses_host_end(ulysses_t h, void* stream);
+
+/*
  * ulysses_get_status — read and clear the handle's device status word.
  * Synchronises the device. Returns ULYSSES_OK, ULYSSES_ERR_TIMEOUT if a
  * bounded device-side wait ran out since the last call (the kernel then

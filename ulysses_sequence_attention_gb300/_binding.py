@@ -75,6 +75,12 @@ lib.ulysses_layer_bwd.argtypes = [_vp] + [_pp] * 9 + [_vp, _vp]
 lib.ulysses_layer_bwd.restype = ctypes.c_int
 lib.ulysses_fused_supported.argtypes = [_vp]
 lib.ulysses_fused_supported.restype = ctypes.c_int
+lib.ulysses_host_begin.argtypes = [_vp, _vp]
+lib.ulysses_host_begin.restype = ctypes.c_int
+lib.ulysses_host_end.argtypes = [_vp, _vp]
+lib.ulysses_host_end.restype = ctypes.c_int
+lib.ulysses_host_step.argtypes = [_vp, ctypes.c_int, _pp, _pp, _pp, _pp, _vp, _vp]
+lib.ulysses_host_step.restype = ctypes.c_int
 lib.ulysses_get_status.argtypes = [_vp]
 lib.ulysses_get_status.restype = ctypes.c_int
 lib.ulysses_attn_bwd_noalloc.argtypes = [_vp] + [_pp] * 9 + [_vp]
@@ -274,6 +280,53 @@ def ulysses_layer_bwd(h: UlyssesHandle, q, k, v, o, do, lse, dq, dk, dv, workspa
             _ptrs(h, lse, h.bs * h.Hq * h.sl, torch.float32, "lse"),
             _ptrs(h, dq, nq, dt, "dq"), _ptrs(h, dk, nk, dt, "dk"), _ptrs(h, dv, nk, dt, "dv")]
     _check(lib.ulysses_layer_bwd(h.ptr, *args, ws, _stream(stream)), "ulysses_layer_bwd")
+
+
+def _host_ptrs(groups, numels, dtype, name):
+    """HOST pointers of the tensors of each group, in order (CPU tensors, contiguous)."""
+    flat = []
+    for g, (tensors, numel) in enumerate(zip(groups, numels)):
+        for r, t in enumerate(tensors):
+            if t.device.type != "cpu" or not t.is_contiguous() or t.dtype != dtype or t.numel() != numel:
+                raise ValueError(f"{name}[{g}][{r}]: expected a contiguous CPU {dtype} tensor of {numel} elements")
+            flat.append(t.data_ptr())
+    arr = (_vp * len(flat))(*flat)
+    return ctypes.cast(arr, _pp)
+
+
+def ulysses_host_begin(h: UlyssesHandle, stream=None):
+    """The handle's copy streams wait for the work already enqueued on `stream`."""
+    _check(lib.ulysses_host_begin(h.ptr, _stream(stream)), "ulysses_host_begin")
+
+
+def ulysses_host_end(h: UlyssesHandle, stream=None):
+    """`stream` waits for every copy of the host steps enqueued so far."""
+    _check(lib.ulysses_host_end(h.ptr, _stream(stream)), "ulysses_host_end")
+
+
+def ulysses_host_step(h: UlyssesHandle, slot: int, host_in, host_out, dev, lse, workspace, stream=None):
+    """One fwd+bwd step from host shards to host shards (see the C header).
+
+    host_in: [q, k, v, do] and host_out: [o, dq, dk, dv], each a list of P CPU
+    tensors (pinned for overlap). dev: [q, k, v, do, o, dq, dk, dv], each a
+    list of P device tensors: the slot's buffers.
+    """
+    dt = h.torch_dtype
+    n = h.sl // h.P
+    nq = n * h.bs * h.hc * h.hs
+    nk = n * h.bs * h.hkv * h.hs
+    sizes_in = [nq, nk, nk, nq]
+    sizes_out = [nq, nq, nk, nk]
+    hin = _host_ptrs(host_in, sizes_in, dt, "host_in")
+    hout = _host_ptrs(host_out, sizes_out, dt, "host_out")
+    flat = []
+    for g, (tensors, numel) in enumerate(zip(dev, sizes_in + sizes_out)):
+        p = _ptrs(h, tensors, numel, dt, f"dev[{g}]")
+        flat.extend(p[r] for r in range(h.P))
+    darr = (_vp * len(flat))(*flat)
+    _check(lib.ulysses_host_step(h.ptr, int(slot), hin, hout, ctypes.cast(darr, _pp),
+                                 _ptrs(h, lse, h.bs * h.Hq * h.sl, torch.float32, "lse"),
+                                 _workspace_ptr(h, workspace), _stream(stream)), "ulysses_host_step")
 
 
 def ulysses_get_status(h: UlyssesHandle) -> int:

@@ -160,6 +160,7 @@ int ulysses_create(ulysses_t* out, int64_t sl, int64_t bs, int hc, int hkv, int 
 void ulysses_destroy(ulysses_t h) {
   Layer* L = reinterpret_cast<Layer*>(h);
   if (!L) return;
+  uly::destroy_host_pipe(*L);
   cudaFree(L->d_status);
   cudaFree(L->d_doc_offsets);
   cudaFree(L->d_kvp_range);

@@ -134,6 +134,15 @@ struct Layer {
   long long timeout_cycles = 4000000000LL;  // bound of every device-side wait (~2 s)
   int inject_fault = 0;                     // test hook (ulysses_inject_fault)
   mutable Timing timing;                    // ulysses_timing_enable / ulysses_timing_read
+  // Host-streaming steps (ulysses_host_begin / _step / _end): two copy
+  // streams and, per device-buffer slot, the events that order its reuse.
+  // Created on first use, destroyed with the handle.
+  struct HostPipe {
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t qkv_in[2] = {}, do_in[2] = {}, o_done[2] = {}, computed[2] = {}, out_copied[2] = {};
+    cudaEvent_t fork = nullptr, h2d_tail = nullptr, d2h_tail = nullptr;
+    bool ready = false;
+  } pipe;
   int64_t n() const { return sl / P; }          // tokens per sequence shard
   int esize() const { return dtype == ULYSSES_BF16 ? 2 : 4; }
   bool empty() const { return sl == 0 || bs == 0; }
@@ -201,6 +210,9 @@ inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? ULYSSES_OK : U
 
 // Adds n to the library-wide kernel launch counter (ulysses_launch_count).
 void count_launches(int n);
+
+// Frees the host-streaming streams and events of a handle (host_step.cu).
+void destroy_host_pipe(Layer& L);
 
 }  // namespace uly
 

@@ -18,6 +18,10 @@ Two ways to run them, both through the C-ABI of libulysses.so:
 
 Both give bit-identical results. This class only owns the intermediate buffers
 (torch device memory) and enqueues the calls on the current stream.
+
+HostSteps runs whole training steps from host memory (ulysses_host_*): inputs
+in, forward and backward, outputs out, with the copies overlapped with the
+neighbouring steps' kernels.
 """
 from __future__ import annotations
 
@@ -114,3 +118,53 @@ class UlyssesLayer:
     @property
     def head_buffers(self):
         return self._bufs
+
+
+class HostSteps:
+    """Training steps of a layer from host memory, copies overlapped with compute.
+
+    Wraps ulysses_host_begin / ulysses_host_step / ulysses_host_end: the
+    inputs (Q, K, V, dO sequence shards) come from host tensors and the
+    outputs (O, dQ, dK, dV) go back to host tensors. Two slots of device
+    buffers alternate, so one step's copies overlap its neighbours' kernels.
+    Needs a shape that ulysses_fused_supported accepts.
+
+        hs = HostSteps(layer)
+        hs.begin()
+        for batch, out in zip(batches, outs):   # dicts of lists of P CPU tensors
+            hs.step(batch, out)
+        hs.end()
+        torch.cuda.current_stream().synchronize()   # outs are valid now
+    """
+
+    IN = ("q", "k", "v", "do")
+    OUT = ("o", "dq", "dk", "dv")
+
+    def __init__(self, layer: UlyssesLayer):
+        if not layer.fused:
+            raise B.UlyssesError(B.ULYSSES_ERR_UNSUPPORTED, "HostSteps needs the fused layer path")
+        self.L = layer
+        heads = {"q": layer.hc, "k": layer.hkv, "v": layer.hkv, "do": layer.hc,
+                 "o": layer.hc, "dq": layer.hc, "dk": layer.hkv, "dv": layer.hkv}
+        self.slots = [{n: layer.new_seq_shards(H) for n, H in heads.items()} for _ in range(2)]
+        b = layer._alloc(backward=True)
+        self.lse, self.ws = b["lse"], b["ws"]
+        self.i = 0
+
+    def host_bytes_per_step(self):
+        """(host->device, device->host) bytes that one step copies."""
+        per = lambda names: sum(t.numel() * t.element_size() for n in names for t in self.slots[0][n])  # noqa: E731
+        return per(self.IN), per(self.OUT)
+
+    def begin(self, stream=None):
+        B.ulysses_host_begin(self.L.h, stream)
+
+    def step(self, host_in, host_out, stream=None):
+        s = self.slots[self.i % 2]
+        dev = [s[n] for n in self.IN + self.OUT]
+        B.ulysses_host_step(self.L.h, self.i % 2, [host_in[n] for n in self.IN], [host_out[n] for n in self.OUT],
+                            dev, self.lse, self.ws, stream)
+        self.i += 1
+
+    def end(self, stream=None):
+        B.ulysses_host_end(self.L.h, stream)
