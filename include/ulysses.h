@@ -64,7 +64,7 @@ typedef enum ulysses_status {
   ULYSSES_ERR_UNSUPPORTED = -4,  /* valid for the method, but outside what this build implements */
   ULYSSES_ERR_CUDA = -5,         /* a CUDA runtime call failed (allocation, launch) */
   ULYSSES_ERR_TIMEOUT = -6,      /* a device-side bounded wait ran out (reported by ulysses_get_status) */
-  ULYSSES_ERR_TOO_LARGE = -7     /* ulysses_attn_bwd_noalloc: the call needs more scratch than the library holds */
+  ULYSSES_ERR_TOO_LARGE = -7     /* beyond a fixed size: the scratch of ulysses_attn_bwd_noalloc, the capacity of ulysses_set_seq */
 } ulysses_status;
 
 typedef enum ulysses_dtype {
@@ -103,6 +103,47 @@ typedef enum ulysses_dtype {
 int ulysses_create(ulysses_t* out, int64_t sl, int64_t bs, int hc, int hkv, int hs, int P,
                    int causal, const int32_t* doc_offsets, int ndoc, int dtype);
 
+/*
+ * ulysses_create_varlen — a handle for batches of varying sequence length:
+ * the pages' `seq_length_is_variable=True` mode (ALST guide, section 2.1 item
+ * (5); HF blog, the DeepSpeedSequenceParallelConfig options). ulysses_create is
+ * the fixed mode (`seq_length_is_variable=False`), whose shapes are computed
+ * once.
+ *
+ *   max_sl    the longest sequence the handle will take (capacity).
+ *   max_docs  the most documents a sequence may be packed from (>= 1).
+ *   others    as for ulysses_create; the same shape and divisibility rules,
+ *             except that sl % P is checked per sequence by ulysses_set_seq.
+ * The handle starts empty (sl = 0): every call is a no-op until the first
+ * ulysses_set_seq. Its device tables are sized for the capacity, and
+ * ulysses_workspace_size reports the workspace for max_sl, so one set of
+ * buffers serves every sequence. Allocates a few bytes of device memory per
+ * 256 tokens of capacity on the current device.
+ */
+int ulysses_create_varlen(ulysses_t* out, int64_t max_sl, int64_t bs, int hc, int hkv, int hs, int P,
+                          int causal, int max_docs, int dtype);
+
+/*
+ * ulysses_set_seq — switch a handle to a new sequence: length and document
+ * offsets. Works on any handle within its capacity (ulysses_create's capacity
+ * is its own sl and document count).
+ *
+ *   sl           new global sequence length, 0 <= sl <= capacity, sl % P == 0
+ *                (ULYSSES_ERR_DIVISIBILITY otherwise; ULYSSES_ERR_TOO_LARGE
+ *                above the capacity). 0 makes every call a no-op.
+ *   doc_offsets  HOST array of ndoc+1 offsets as for ulysses_create, with
+ *                ndoc <= max_docs; or NULL (one document).
+ *   stream       the new tile schedule and offsets are copied to the device in
+ *                order on this stream. Calls enqueued after this one on the same
+ *                stream use the new sequence; work of this handle already
+ *                enqueued on other streams must be finished or ordered before
+ *                `stream`. The host arrays may be freed on return.
+ * Buffers passed to later calls take the new sl: a sequence shard is
+ * [sl/P][bs][H][hs], a head shard [sl][bs][H/P][hs], LSE [bs][hc/P][sl].
+ * Allocates nothing. A failed check changes nothing and enqueues nothing.
+ */
+int ulysses_set_seq(ulysses_t h, int64_t sl, const int32_t* doc_offsets, int ndoc, void* stream);
+
 /* Free the handle and its device metadata. NULL is a no-op. The caller must
  * make sure that no work using the handle is still running. */
 void ulysses_destroy(ulysses_t h);
@@ -111,7 +152,8 @@ void ulysses_destroy(ulysses_t h);
 const char* ulysses_strerror(int status);
 
 /*
- * ulysses_workspace_size — bytes of device workspace that ulysses_attn_bwd needs.
+ * ulysses_workspace_size — bytes of device workspace that ulysses_attn_bwd needs,
+ * at the handle's capacity (its sl; max_sl for ulysses_create_varlen).
  * bf16 with hs = 128 (the tensor-core path): for each rank, two fp32 row
  * planes [bs][hc/P][pitch], -LSE*log2(e) and D = rowsum(dO * O), where pitch
  * is sl rounded up to a multiple of 4: P * 2 * bs * (hc/P) * pitch * 4 bytes.

@@ -136,3 +136,38 @@ def test_binding_argument_counts_match_the_header(u):
         fn = getattr(u._binding.lib, name)
         assert fn.argtypes is not None, name
         assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+
+
+def _varlen_status(u, **kw):
+    args = dict(max_sl=4096, bs=1, hc=32, hkv=8, hs=128, P=8, causal=True, max_docs=4, dtype="bf16")
+    args.update(kw)
+    try:
+        u.ulysses_create_varlen(**args).destroy()
+        return u.ULYSSES_OK
+    except u.UlyssesError as e:
+        return e.status
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(max_docs=0), "INVALID_ARG"),
+    (dict(max_sl=-1), "INVALID_ARG"),
+    (dict(hc=30), "DIVISIBILITY"),          # heads not divisible by the degree
+    (dict(hkv=3, hc=30, P=2), "DIVISIBILITY"),  # kv heads neither divide nor are divided by P
+    (dict(hs=80), "UNSUPPORTED"),
+    (dict(max_sl=(1 << 30) + 8), "UNSUPPORTED"),
+])
+def test_varlen_create_rejections(u, kw, expect):
+    """The varying-length handle applies the same head rules as the fixed one, before any device call."""
+    assert _varlen_status(u, **kw) == getattr(u, "ULYSSES_ERR_" + expect)
+
+
+def test_varlen_capacity_need_not_divide_by_the_degree(u):
+    # sl % P is a rule on each sequence (checked by ulysses_set_seq), not on the capacity
+    st = _varlen_status(u, max_sl=4100)
+    assert st in (u.ULYSSES_OK, u.ULYSSES_ERR_CUDA)   # no GPU here: it gets as far as the allocation
+
+
+def test_set_seq_rejects_a_null_handle(u):
+    assert u._binding.lib.ulysses_set_seq(None, 128, None, 0, None) == u.ULYSSES_ERR_INVALID_ARG
+    assert u._binding.lib.ulysses_host_begin(None, None) == u.ULYSSES_ERR_INVALID_ARG
+    assert u._binding.lib.ulysses_host_end(None, None) == u.ULYSSES_ERR_INVALID_ARG

@@ -14,6 +14,6 @@ from ._binding import (  # noqa: F401
     ulysses_strerror, ulysses_workspace_size, ulysses_set_wait_limit, ulysses_inject_fault,
     ulysses_timing_enable, ulysses_timing_read, ULYSSES_KERNEL_COUNT, KERNEL_NAMES,
     ulysses_fused_supported, ulysses_layer_fwd, ulysses_layer_bwd,
-    ulysses_host_begin, ulysses_host_step, ulysses_host_end,
+    ulysses_host_begin, ulysses_host_step, ulysses_host_end, ulysses_create_varlen, ulysses_set_seq,
 )
 from .layer import HostSteps, UlyssesLayer  # noqa: F401

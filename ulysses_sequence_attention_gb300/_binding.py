@@ -55,6 +55,12 @@ lib.ulysses_create.argtypes = [ctypes.POINTER(_vp), ctypes.c_int64, ctypes.c_int
                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                ctypes.POINTER(ctypes.c_int32), ctypes.c_int, ctypes.c_int]
 lib.ulysses_create.restype = ctypes.c_int
+lib.ulysses_create_varlen.argtypes = [ctypes.POINTER(_vp), ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int]
+lib.ulysses_create_varlen.restype = ctypes.c_int
+lib.ulysses_set_seq.argtypes = [_vp, ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), ctypes.c_int, _vp]
+lib.ulysses_set_seq.restype = ctypes.c_int
 lib.ulysses_destroy.argtypes = [_vp]
 lib.ulysses_destroy.restype = None
 lib.ulysses_strerror.argtypes = [ctypes.c_int]
@@ -159,6 +165,31 @@ def ulysses_create(sl: int, bs: int, hc: int, hkv: int, hs: int, P: int, causal:
     _check(st, "ulysses_create")
     return UlyssesHandle(out.value, sl, bs, hc, hkv, hs, P, bool(causal),
                          None if doc_offsets is None else list(doc_offsets), dt)
+
+
+def ulysses_create_varlen(max_sl: int, bs: int, hc: int, hkv: int, hs: int, P: int, causal: bool = True,
+                          max_docs: int = 1, dtype="bf16") -> UlyssesHandle:
+    """A handle for sequences of varying length up to max_sl; empty until ulysses_set_seq."""
+    dt = _DTYPES.get(dtype, dtype)
+    out = _vp()
+    st = lib.ulysses_create_varlen(ctypes.byref(out), int(max_sl), int(bs), int(hc), int(hkv), int(hs), int(P),
+                                   int(bool(causal)), int(max_docs), int(dt))
+    _check(st, "ulysses_create_varlen")
+    h = UlyssesHandle(out.value, 0, bs, hc, hkv, hs, P, bool(causal), None, dt)
+    h.max_sl, h.max_docs = int(max_sl), int(max_docs)
+    return h
+
+
+def ulysses_set_seq(h: UlyssesHandle, sl: int, doc_offsets: Optional[Sequence[int]] = None, stream=None):
+    """Switch h to a new sequence (length and document offsets), in order on `stream`."""
+    if doc_offsets is not None:
+        offs = (ctypes.c_int32 * len(doc_offsets))(*[int(x) for x in doc_offsets])
+        nd = len(doc_offsets) - 1
+    else:
+        offs, nd = None, 0
+    _check(lib.ulysses_set_seq(h.ptr, int(sl), offs, nd, _stream(stream)), "ulysses_set_seq")
+    h.sl = int(sl)
+    h.doc_offsets = None if doc_offsets is None else list(doc_offsets)
 
 
 def ulysses_destroy(h: UlyssesHandle):

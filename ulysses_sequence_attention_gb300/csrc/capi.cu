@@ -51,6 +51,126 @@ static int check_ptrs(const void* const* ptrs, int P) {
   return ULYSSES_OK;
 }
 
+// Shape rules that do not depend on the sequence length.
+static int check_shape(int64_t sl_cap, int64_t bs, int hc, int hkv, int hs, int P, int causal, int dtype) {
+  if (sl_cap < 0 || bs < 0 || hc <= 0 || hkv <= 0 || hs <= 0 || P <= 0) return ULYSSES_ERR_INVALID_ARG;
+  if (dtype != ULYSSES_BF16 && dtype != ULYSSES_FP32) return ULYSSES_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ULYSSES_ERR_INVALID_ARG;
+  // Divisibility rules of the method.
+  if (hc % P != 0) return ULYSSES_ERR_DIVISIBILITY;
+  if (hc % hkv != 0) return ULYSSES_ERR_DIVISIBILITY;
+  if (hkv % P != 0 && P % hkv != 0) return ULYSSES_ERR_DIVISIBILITY;
+  // Limits of this build.
+  if (P > ULYSSES_MAX_P) return ULYSSES_ERR_UNSUPPORTED;
+  if (hs != 32 && hs != 64 && hs != 128) return ULYSSES_ERR_UNSUPPORTED;
+  if (sl_cap > (int64_t(1) << 30) || bs > 65535) return ULYSSES_ERR_UNSUPPORTED;
+  const int64_t esize = dtype == ULYSSES_BF16 ? 2 : 4;
+  if (sl_cap * bs * (int64_t)hc * hs * esize > (int64_t(1) << 38)) return ULYSSES_ERR_UNSUPPORTED;
+  return ULYSSES_OK;
+}
+
+// Rules on one sequence: sl % P (ALST guide 2.1 (5): the sequence length
+// divisible by sp_size) and the document offsets, at which position ids
+// restart (ALST guide 2.2).
+static int check_seq(int64_t sl, int64_t cap_sl, int P, const int32_t* offs, int ndoc, int cap_docs) {
+  if (sl < 0 || sl > cap_sl) return ULYSSES_ERR_INVALID_ARG;
+  if (sl % P != 0) return ULYSSES_ERR_DIVISIBILITY;
+  if (offs) {
+    if (ndoc < 1 || ndoc > cap_docs || offs[0] != 0 || offs[ndoc] != sl) return ULYSSES_ERR_INVALID_ARG;
+    for (int d = 0; d < ndoc; ++d)
+      if (offs[d + 1] <= offs[d]) return ULYSSES_ERR_INVALID_ARG;
+  } else if (ndoc != 0 && ndoc != 1) {
+    return ULYSSES_ERR_INVALID_ARG;
+  }
+  return ULYSSES_OK;
+}
+
+static void set_offsets(Layer& L, int64_t sl, const int32_t* offs, int ndoc) {
+  L.sl = sl;
+  if (offs) {
+    L.ndoc = ndoc;
+    L.doc_offsets.assign(offs, offs + ndoc + 1);
+  } else {
+    L.ndoc = 1;
+    L.doc_offsets = {0, (int32_t)sl};
+  }
+}
+
+// Copies the document offsets and, for the tensor-core path, the pair-tile
+// schedules of the current sequence into the handle's device tables, which
+// hold the capacity. async: in order on `stream` (the host vectors are
+// pageable, so each copy has left them when cudaMemcpyAsync returns).
+static cudaError_t upload_seq(Layer& L, cudaStream_t stream, bool async) {
+  if (L.empty()) return cudaSuccess;
+  auto copy = [&](void* dst, const void* src, size_t bytes) {
+    return async ? cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, stream)
+                 : cudaMemcpy(dst, src, bytes, cudaMemcpyHostToDevice);
+  };
+  cudaError_t e = copy(L.d_doc_offsets, L.doc_offsets.data(), sizeof(int32_t) * (L.ndoc + 1));
+  if (e == cudaSuccess && uly::fwd_sm103_supported(L)) {
+    std::vector<int2> kvp, qp;
+    std::vector<int> kvo, qo;
+    uly::plan_pair_tiles(L, kvp, kvo, qp, qo);
+    if (e == cudaSuccess) e = copy(L.d_kvp_range, kvp.data(), sizeof(int2) * kvp.size());
+    if (e == cudaSuccess) e = copy(L.d_kvp_order, kvo.data(), sizeof(int) * kvo.size());
+    if (e == cudaSuccess) e = copy(L.d_qp_range, qp.data(), sizeof(int2) * qp.size());
+    if (e == cudaSuccess) e = copy(L.d_qp_order, qo.data(), sizeof(int) * qo.size());
+  }
+  return e;
+}
+
+static void free_layer(Layer* L) {
+  uly::destroy_host_pipe(*L);
+  cudaFree(L->d_status);
+  cudaFree(L->d_doc_offsets);
+  cudaFree(L->d_kvp_range);
+  cudaFree(L->d_kvp_order);
+  cudaFree(L->d_qp_range);
+  cudaFree(L->d_qp_order);
+  delete L;
+}
+
+// A handle whose device tables hold sequences up to cap_sl tokens in up to
+// cap_docs documents, set to the sequence (sl, offs).
+static int create_layer(ulysses_t* out, int64_t sl, int64_t bs, int hc, int hkv, int hs, int P, int causal,
+                        const int32_t* offs, int ndoc, int dtype, int64_t cap_sl, int cap_docs) {
+  Layer* L = new (std::nothrow) Layer();
+  if (!L) return ULYSSES_ERR_INVALID_ARG;
+  L->bs = bs;
+  L->hc = hc;
+  L->hkv = hkv;
+  L->hs = hs;
+  L->P = P;
+  L->causal = causal;
+  L->dtype = dtype;
+  L->Hq = hc / P;
+  L->Hk = hkv % P == 0 ? hkv / P : 1;
+  L->cap_sl = cap_sl;
+  L->cap_docs = cap_docs;
+  set_offsets(*L, sl, offs, ndoc);
+  if (cudaGetDevice(&L->device) != cudaSuccess) {
+    delete L;
+    return ULYSSES_ERR_CUDA;
+  }
+  cudaError_t e = cudaMalloc(&L->d_status, sizeof(unsigned));
+  if (e == cudaSuccess) e = cudaMemset(L->d_status, 0, sizeof(unsigned));
+  if (e == cudaSuccess) e = cudaMalloc(&L->d_doc_offsets, sizeof(int32_t) * (cap_docs + 1));
+  if (e == cudaSuccess && uly::fwd_sm103_supported(*L) && cap_sl > 0 && bs > 0) {
+    const size_t n_pair = (size_t)((cap_sl + 255) / 256);
+    e = cudaMalloc(&L->d_kvp_range, sizeof(int2) * n_pair);
+    if (e == cudaSuccess) e = cudaMalloc(&L->d_kvp_order, sizeof(int) * n_pair);
+    if (e == cudaSuccess) e = cudaMalloc(&L->d_qp_range, sizeof(int2) * n_pair);
+    if (e == cudaSuccess) e = cudaMalloc(&L->d_qp_order, sizeof(int) * n_pair);
+  }
+  if (e == cudaSuccess) e = upload_seq(*L, 0, false);
+  if (e != cudaSuccess) {
+    free_layer(L);
+    return ULYSSES_ERR_CUDA;
+  }
+  *out = reinterpret_cast<ulysses_t>(L);
+  return ULYSSES_OK;
+}
+
 #define CHECK_PTRS(arr)                                             \
   do {                                                              \
     int _st = check_ptrs((const void* const*)(arr), L->P);          \
@@ -68,7 +188,7 @@ const char* ulysses_strerror(int status) {
     case ULYSSES_ERR_UNSUPPORTED: return "unsupported configuration";
     case ULYSSES_ERR_CUDA: return "CUDA runtime error";
     case ULYSSES_ERR_TIMEOUT: return "device-side wait timed out";
-    case ULYSSES_ERR_TOO_LARGE: return "the backward needs more scratch than the library's built-in array";
+    case ULYSSES_ERR_TOO_LARGE: return "larger than a fixed limit (built-in backward scratch, or the handle's capacity)";
     default: return "unknown status";
   }
 }
@@ -77,97 +197,38 @@ int ulysses_create(ulysses_t* out, int64_t sl, int64_t bs, int hc, int hkv, int 
                    int causal, const int32_t* doc_offsets, int ndoc, int dtype) {
   if (!out) return ULYSSES_ERR_INVALID_ARG;
   *out = nullptr;
-  if (sl < 0 || bs < 0 || hc <= 0 || hkv <= 0 || hs <= 0 || P <= 0) return ULYSSES_ERR_INVALID_ARG;
-  if (dtype != ULYSSES_BF16 && dtype != ULYSSES_FP32) return ULYSSES_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return ULYSSES_ERR_INVALID_ARG;
-  // Divisibility rules of the method.
-  if (hc % P != 0) return ULYSSES_ERR_DIVISIBILITY;
-  if (sl % P != 0) return ULYSSES_ERR_DIVISIBILITY;
-  if (hc % hkv != 0) return ULYSSES_ERR_DIVISIBILITY;
-  if (hkv % P != 0 && P % hkv != 0) return ULYSSES_ERR_DIVISIBILITY;
-  // Limits of this build.
-  if (P > ULYSSES_MAX_P) return ULYSSES_ERR_UNSUPPORTED;
-  if (hs != 32 && hs != 64 && hs != 128) return ULYSSES_ERR_UNSUPPORTED;
-  if (sl > (int64_t(1) << 30) || bs > 65535) return ULYSSES_ERR_UNSUPPORTED;
-  const int64_t esize = dtype == ULYSSES_BF16 ? 2 : 4;
-  if (sl * bs * (int64_t)hc * hs * esize > (int64_t(1) << 38)) return ULYSSES_ERR_UNSUPPORTED;
-  // Document offsets: position ids restart at every offset (ALST guide, section 2.2).
-  if (doc_offsets) {
-    if (ndoc < 1 || doc_offsets[0] != 0 || doc_offsets[ndoc] != sl) return ULYSSES_ERR_INVALID_ARG;
-    for (int d = 0; d < ndoc; ++d)
-      if (doc_offsets[d + 1] <= doc_offsets[d]) return ULYSSES_ERR_INVALID_ARG;
-  } else if (ndoc != 0 && ndoc != 1) {
-    return ULYSSES_ERR_INVALID_ARG;
-  }
+  int st = check_shape(sl, bs, hc, hkv, hs, P, causal, dtype);
+  if (st != ULYSSES_OK) return st;
+  st = check_seq(sl, sl, P, doc_offsets, ndoc, doc_offsets ? ndoc : 1);
+  if (st != ULYSSES_OK) return st;
+  return create_layer(out, sl, bs, hc, hkv, hs, P, causal, doc_offsets, ndoc, dtype, sl, doc_offsets ? ndoc : 1);
+}
 
-  Layer* L = new (std::nothrow) Layer();
+int ulysses_create_varlen(ulysses_t* out, int64_t max_sl, int64_t bs, int hc, int hkv, int hs, int P, int causal,
+                          int max_docs, int dtype) {
+  if (!out) return ULYSSES_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (max_docs < 1) return ULYSSES_ERR_INVALID_ARG;
+  int st = check_shape(max_sl, bs, hc, hkv, hs, P, causal, dtype);
+  if (st != ULYSSES_OK) return st;
+  // Starts empty (sl = 0): every call is a no-op until ulysses_set_seq.
+  return create_layer(out, 0, bs, hc, hkv, hs, P, causal, nullptr, 0, dtype, max_sl, max_docs);
+}
+
+int ulysses_set_seq(ulysses_t h, int64_t sl, const int32_t* doc_offsets, int ndoc, void* stream) {
+  Layer* L = reinterpret_cast<Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
-  L->sl = sl;
-  L->bs = bs;
-  L->hc = hc;
-  L->hkv = hkv;
-  L->hs = hs;
-  L->P = P;
-  L->causal = causal;
-  L->dtype = dtype;
-  L->Hq = hc / P;
-  L->Hk = hkv % P == 0 ? hkv / P : 1;
-  if (doc_offsets) {
-    L->ndoc = ndoc;
-    L->doc_offsets.assign(doc_offsets, doc_offsets + ndoc + 1);
-  } else {
-    L->ndoc = 1;
-    L->doc_offsets = {0, (int32_t)sl};
-  }
-  if (cudaGetDevice(&L->device) != cudaSuccess) {
-    delete L;
-    return ULYSSES_ERR_CUDA;
-  }
-  cudaError_t e = cudaMalloc(&L->d_status, sizeof(unsigned));
-  if (e == cudaSuccess) e = cudaMemset(L->d_status, 0, sizeof(unsigned));
-  if (e == cudaSuccess) e = cudaMalloc(&L->d_doc_offsets, sizeof(int32_t) * (L->ndoc + 1));
-  if (e == cudaSuccess)
-    e = cudaMemcpy(L->d_doc_offsets, L->doc_offsets.data(), sizeof(int32_t) * (L->ndoc + 1),
-                   cudaMemcpyHostToDevice);
-  if (e == cudaSuccess && uly::fwd_sm103_supported(*L) && !L->empty()) {
-    std::vector<int2> kvp, qp;
-    std::vector<int> kvo, qo;
-    uly::plan_pair_tiles(*L, kvp, kvo, qp, qo);
-    auto upload = [&](auto** dst, const auto& v) {
-      using T = typename std::decay_t<decltype(v)>::value_type;
-      if (e == cudaSuccess) e = cudaMalloc(dst, sizeof(T) * v.size());
-      if (e == cudaSuccess) e = cudaMemcpy(*dst, v.data(), sizeof(T) * v.size(), cudaMemcpyHostToDevice);
-    };
-    upload(&L->d_kvp_range, kvp);
-    upload(&L->d_kvp_order, kvo);
-    upload(&L->d_qp_range, qp);
-    upload(&L->d_qp_order, qo);
-  }
-  if (e != cudaSuccess) {
-    cudaFree(L->d_status);
-    cudaFree(L->d_doc_offsets);
-    cudaFree(L->d_kvp_range);
-    cudaFree(L->d_kvp_order);
-    cudaFree(L->d_qp_range);
-    cudaFree(L->d_qp_order);
-    delete L;
-    return ULYSSES_ERR_CUDA;
-  }
-  *out = reinterpret_cast<ulysses_t>(L);
-  return ULYSSES_OK;
+  if (sl > L->cap_sl) return ULYSSES_ERR_TOO_LARGE;
+  int st = check_seq(sl, L->cap_sl, L->P, doc_offsets, ndoc, L->cap_docs);
+  if (st != ULYSSES_OK) return st;
+  set_offsets(*L, sl, doc_offsets, ndoc);
+  return uly::cuda_status(upload_seq(*L, (cudaStream_t)stream, true));
 }
 
 void ulysses_destroy(ulysses_t h) {
   Layer* L = reinterpret_cast<Layer*>(h);
   if (!L) return;
-  uly::destroy_host_pipe(*L);
-  cudaFree(L->d_status);
-  cudaFree(L->d_doc_offsets);
-  cudaFree(L->d_kvp_range);
-  cudaFree(L->d_kvp_order);
-  cudaFree(L->d_qp_range);
-  cudaFree(L->d_qp_order);
-  delete L;
+  free_layer(L);
 }
 
 int ulysses_workspace_size(ulysses_t h, size_t* bytes) {
@@ -176,8 +237,17 @@ int ulysses_workspace_size(ulysses_t h, size_t* bytes) {
   // Tensor-core path: per rank two fp32 row planes, -LSE*log2(e) and
   // D = rowsum(dO * O), [bs][Hq][sl rounded up to 4] each. Other paths: D only,
   // [P][bs][Hq][sl].
-  *bytes = uly::fwd_sm103_supported(*L) ? uly::bwd_sm103_workspace(*L)
-                                        : (size_t)L->P * L->bs * L->Hq * L->sl * sizeof(float);
+  // Sized for the handle's capacity (its own sl unless made by
+  // ulysses_create_varlen), so one workspace serves every ulysses_set_seq.
+  Layer cap;
+  cap.sl = L->cap_sl;
+  cap.bs = L->bs;
+  cap.P = L->P;
+  cap.Hq = L->Hq;
+  cap.hs = L->hs;
+  cap.dtype = L->dtype;
+  *bytes = uly::fwd_sm103_supported(cap) ? uly::bwd_sm103_workspace(cap)
+                                         : (size_t)cap.P * cap.bs * cap.Hq * cap.sl * sizeof(float);
   return ULYSSES_OK;
 }
 

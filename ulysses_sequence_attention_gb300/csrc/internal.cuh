@@ -119,6 +119,8 @@ struct Layer {
   int Hq = 0;       // query heads per rank (hc / P)
   int Hk = 0;       // kv heads per rank (hkv / P, or 1 when replicated)
   int ndoc = 1;
+  int64_t cap_sl = 0;                 // device tables hold sequences up to cap_sl tokens
+  int cap_docs = 1;                   // ... in up to cap_docs documents
   std::vector<int32_t> doc_offsets;   // host copy, ndoc + 1 entries
   int32_t* d_doc_offsets = nullptr;   // device copy, ndoc + 1 entries
   unsigned* d_status = nullptr;       // device status word

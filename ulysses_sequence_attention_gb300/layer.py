@@ -25,6 +25,7 @@ neighbouring steps' kernels.
 """
 from __future__ import annotations
 
+import math
 from typing import List, Optional, Sequence
 
 import torch
@@ -35,37 +36,69 @@ from . import _binding as B
 class UlyssesLayer:
     def __init__(self, sl: int, bs: int, hc: int, hkv: int, hs: int, P: int, causal: bool = True,
                  doc_offsets: Optional[Sequence[int]] = None, dtype=torch.bfloat16,
-                 device: str = "cuda", fused: Optional[bool] = None):
+                 device: str = "cuda", fused: Optional[bool] = None, _handle=None):
         """fused: None picks the fused path when the shape allows it; True requires it."""
-        self.h = B.ulysses_create(sl, bs, hc, hkv, hs, P, causal, doc_offsets, dtype)
+        self.h = _handle or B.ulysses_create(sl, bs, hc, hkv, hs, P, causal, doc_offsets, dtype)
+        self.cap_sl = getattr(self.h, "max_sl", sl)
         self.sl, self.bs, self.hc, self.hkv, self.hs, self.P = sl, bs, hc, hkv, hs, P
         self.dtype = dtype
         self.device = device
         self.Hq, self.Hk = self.h.Hq, self.h.Hk
-        can = B.ulysses_fused_supported(self.h)
-        if fused and not can:
-            raise B.UlyssesError(B.ULYSSES_ERR_UNSUPPORTED, "UlyssesLayer(fused=True)")
-        self.fused = can if fused is None else bool(fused)
+        self._fused_pref = fused
         self._bufs = None
         self._saved = None
+        self._pick_path()
+
+    @classmethod
+    def variable_length(cls, max_sl: int, bs: int, hc: int, hkv: int, hs: int, P: int, causal: bool = True,
+                        max_docs: int = 1, dtype=torch.bfloat16, device: str = "cuda",
+                        fused: Optional[bool] = None) -> "UlyssesLayer":
+        """A layer for batches of varying length (the pages' seq_length_is_variable=True).
+
+        Starts empty; call set_seq before each batch of a new length or packing.
+        Buffers are sized for max_sl once, so a new length allocates nothing.
+        """
+        h = B.ulysses_create_varlen(max_sl, bs, hc, hkv, hs, P, causal, max_docs, dtype)
+        return cls(0, bs, hc, hkv, hs, P, causal, None, dtype, device, fused, _handle=h)
+
+    def set_seq(self, sl: int, doc_offsets: Optional[Sequence[int]] = None, stream=None):
+        """Switch to a sequence of sl tokens (packed at doc_offsets), in order on `stream`."""
+        B.ulysses_set_seq(self.h, sl, doc_offsets, stream)
+        self.sl = sl
+        self._saved = None
+        self._pick_path()
+
+    def _pick_path(self):
+        can = B.ulysses_fused_supported(self.h)
+        if self._fused_pref and not can:
+            raise B.UlyssesError(B.ULYSSES_ERR_UNSUPPORTED, "UlyssesLayer(fused=True)")
+        self.fused = can if self._fused_pref is None else bool(self._fused_pref)
 
     # -- buffers -----------------------------------------------------------
     def _alloc(self, backward: bool):
-        P, sl, bs, hs, dt, dev = self.P, self.sl, self.bs, self.hs, self.dtype, self.device
+        """Intermediate buffers, allocated once for the capacity; views of the current sl."""
+        P, cap, bs, hs, dt, dev = self.P, self.cap_sl, self.bs, self.hs, self.dtype, self.device
 
         def heads(H):
-            return [torch.empty((sl, bs, H, hs), dtype=dt, device=dev) for _ in range(P)]
+            return [torch.empty(cap * bs * H * hs, dtype=dt, device=dev) for _ in range(P)]
 
-        b = self._bufs or {}
-        if "lse" not in b:
-            b["lse"] = [torch.empty((bs, self.Hq, sl), dtype=torch.float32, device=dev) for _ in range(P)]
-        if not self.fused and "qh" not in b:
-            b["qh"], b["kh"], b["vh"], b["oh"] = heads(self.Hq), heads(self.Hk), heads(self.Hk), heads(self.Hq)
-        if backward and "ws" not in b:
+        s = self._store = getattr(self, "_store", None) or {}
+        if "lse" not in s:
+            s["lse"] = [torch.empty(bs * self.Hq * cap, dtype=torch.float32, device=dev) for _ in range(P)]
+        if not self.fused and "qh" not in s:
+            s["qh"], s["kh"], s["vh"], s["oh"] = heads(self.Hq), heads(self.Hk), heads(self.Hk), heads(self.Hq)
+        if backward and "ws" not in s:
             nbytes = B.ulysses_workspace_size(self.h)
-            b["ws"] = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=dev)
-        if backward and not self.fused and "doh" not in b:
-            b["doh"], b["dqh"], b["dkh"], b["dvh"] = heads(self.Hq), heads(self.Hq), heads(self.Hk), heads(self.Hk)
+            s["ws"] = torch.empty((max(nbytes, 16) + 3) // 4, dtype=torch.float32, device=dev)
+        if backward and not self.fused and "doh" not in s:
+            s["doh"], s["dqh"], s["dkh"], s["dvh"] = heads(self.Hq), heads(self.Hq), heads(self.Hk), heads(self.Hk)
+        sl = self.sl
+        shape = {"lse": (bs, self.Hq, sl), "qh": (sl, bs, self.Hq, hs), "oh": (sl, bs, self.Hq, hs),
+                 "doh": (sl, bs, self.Hq, hs), "dqh": (sl, bs, self.Hq, hs), "kh": (sl, bs, self.Hk, hs),
+                 "vh": (sl, bs, self.Hk, hs), "dkh": (sl, bs, self.Hk, hs), "dvh": (sl, bs, self.Hk, hs)}
+        b = {n: [t[:math.prod(shape[n])].view(shape[n]) for t in v] for n, v in s.items() if n != "ws"}
+        if "ws" in s:
+            b["ws"] = s["ws"]
         self._bufs = b
         return b
 
