@@ -130,6 +130,19 @@ def captured_traffic(kernel, workload):
     return None, None
 
 
+def max_over_ranks(ms: float, device, world: int) -> float:
+    """The job's time: the largest of the ranks' times (all ranks get it)."""
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank_step: int, steps: int, world: int, job_ms: float) -> float:
+    """Whole-job throughput: the tokens every rank processed over the job's (slowest rank's) time."""
+    return tokens_per_rank_step * steps * world / (job_ms / 1e3)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -341,14 +354,9 @@ def run_ours(args, w, rank, world):
     s2h_ms = statistics.mean(span("x0", "x1"))
     h2s_ms = statistics.mean(span("x1", "x2"))
 
-    # max over ranks
-    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev, world)
     ms_per_step = elapsed_ms / args.steps
-    tokens = w.sl * w.bs * args.steps * world
-    value = tokens / (elapsed_ms / 1e3)
+    value = job_tokens_per_s(w.sl * w.bs, args.steps, world, elapsed_ms)
 
     e2e = None
     if not args.no_e2e:
@@ -427,12 +435,8 @@ def run_e2e(args, w, L, x, dev, world, barrier):
     t1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
-    ms = t0.elapsed_time(t1)
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms = float(t.item())
-    return {"value": w.sl * w.bs * args.steps * world / (ms / 1e3), "unit": "tokens/s",
+    ms = max_over_ranks(t0.elapsed_time(t1), dev, world)
+    return {"value": job_tokens_per_s(w.sl * w.bs, args.steps, world, ms), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps, "how": how}
 
 
