@@ -511,10 +511,10 @@ constexpr uint32_t kSmem = kOffBar + 256;
 enum {
   B_QO = 0,                  // Q, dO landed (even CTA: + forward)
   B_KFULL = 1,               // NK: key stage landed (even CTA: + forward)
-  B_KEMPTY = B_KFULL + NK,   // NK: key stage consumed (1 compute thread, this CTA)
-  B_S = B_KEMPTY + NK,       // 2: S ready in buffer 0 / 1 (commit, both)
-  B_DP = B_S + 2,            // dP ready (commit, both)
-  B_DS = B_DP + 1,           // even CTA: dS written in both CTAs (16 warps)
+  B_KEMPTY = B_KFULL + NK,   // NK: key stage consumed: dQ of its tile done (commit, both)
+  B_DP = B_KEMPTY + NK,      // S and dP of a tile ready (commit after dP, both)
+  B_SFREE = B_DP + 1,        // even CTA: S copied out of tensor memory in both CTAs (16 warps)
+  B_DS = B_SFREE + 1,        // even CTA: dS written in both CTAs (16 warps)
   B_DONE = B_DS + 1,         // every UMMA done (commit, both)
   B_EPI = B_DONE + 1,        // dQ staged (8 warps)
   B_DRAIN = B_EPI + 1,
@@ -556,7 +556,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t cnt = 1;
       if (i == B_QO || (i >= B_KFULL && i < B_KFULL + NK)) cnt = crank == 0 ? 2 : 1;
       if (i == B_EPI) cnt = 8;
-      if (i == B_DS) cnt = 16;
+      if (i == B_DS || i == B_SFREE) cnt = 16;
       mbar_init(bar(i), cnt);
     }
     fence_mbar_init();
@@ -571,8 +571,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const long long lim = p.timeout;
-  // Tensor memory: S in [0,128) and [128,256) (two buffers), dP in [256,384)
-  // with dS (bf16) written over [256,320), the dQ accumulator in [384,512).
+  // Tensor memory: S in [0,128); dP of tile j in buffer j&1, [128,256) or
+  // [256,384), with dS (bf16) written over the buffer's columns [0,32) and
+  // [64,96); the dQ accumulator in [384,512).
 
   if (warp >= 8) {
     regs_dec<kRegsOther>();
@@ -627,15 +628,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         auto issue_s = [&](int jj) {
           const uint32_t sk = sb + kOffStage + (jj % NK) * kStage;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma2_ss(tmem + (jj & 1) * 128, a_kmaj(sQ, kk), b_kmaj64(sk, kk), id_kk, kk > 0);
-          umma2_commit_both(bar(B_S + (jj & 1)));
+          for (int kk = 0; kk < 8; ++kk) umma2_ss(tmem + 0, a_kmaj(sQ, kk), b_kmaj64(sk, kk), id_kk, kk > 0);
         };
+        // dP of tile jj into buffer jj&1; its commit also covers S of the tile.
         auto issue_dp = [&](int jj) {
           const uint32_t sk = sb + kOffStage + (jj % NK) * kStage;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma2_ss(tmem + 256, a_kmaj(sDO, kk), b_kmaj64(sk + kHalf, kk), id_kk, kk > 0);
+            umma2_ss(tmem + 128 + 128 * (jj & 1), a_kmaj(sDO, kk), b_kmaj64(sk + kHalf, kk), id_kk, kk > 0);
           umma2_commit_both(bar(B_DP));
         };
         bool ok = mbar_wait(bar(B_QO), 0, lim) && mbar_wait(bar(B_KFULL), 0, lim);
@@ -644,23 +644,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           issue_s(0);
           issue_dp(0);
         }
+        // Per key tile jj, in issue order: S and dP of tile jj+1 (once the
+        // compute warps have copied S of tile jj out), then dQ += dS K of
+        // tile jj once its dS is written. The tensor pipe thus runs the next
+        // tile's S and dP while the compute warps form this tile's dS.
         for (int jj = 0; jj < n_kv && ok; ++jj) {
           const int st = jj % NK;
-          const bool next = jj + 1 < n_kv;
-          if (next) {
+          if (jj + 1 < n_kv) {
             const int st1 = (jj + 1) % NK, u1 = (jj + 1) / NK;
-            if (!mbar_wait(bar(B_KFULL + st1), u1 & 1, lim)) { ok = false; break; }
+            if (!mbar_wait(bar(B_KFULL + st1), u1 & 1, lim) || !mbar_wait(bar(B_SFREE), jj & 1, lim)) {
+              ok = false;
+              break;
+            }
             tc_fence_after();
-            issue_s(jj + 1);  // the other S buffer: its last reader finished before dS of jj-1
+            issue_s(jj + 1);
+            issue_dp(jj + 1);  // buffer (jj+1)&1: its dS was read by dQ of tile jj-1, issued before
           }
           if (!mbar_wait(bar(B_DS), jj & 1, lim)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sk = sb + kOffStage + st * kStage;
+          const uint32_t ds = tmem + 128 + 128 * (jj & 1);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dQ += dS K; key half kk/4 of dS at 256 + 64 (kk/4)
-            umma2_ts(tmem + 384, tmem + 256 + (kk >> 2) * 64 + (kk & 3) * 8, b_mn(sk + 2 * kHalf, kk), id_tm,
+          for (int kk = 0; kk < 8; ++kk)  // dQ += dS K; key half kk/4 of dS at +64 (kk/4)
+            umma2_ts(tmem + 384, ds + (kk >> 2) * 64 + (kk & 3) * 8, b_mn(sk + 2 * kHalf, kk), id_tm,
                      (jj > 0 || kk > 0) ? 1u : 0u);
-          if (next) issue_dp(jj + 1);  // overwrites dS only after dQ has read it (issue order)
+          umma2_commit_both(bar(B_KEMPTY + st));  // the key stage is free once dQ has read it
         }
         if (ok)
           umma2_commit_both(bar(B_DONE));
@@ -704,17 +712,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const uint64_t sc2 = f2(p.scale_log2, p.scale_log2), nlp = f2(nl2, nl2), D2 = f2(Di, Di);
+    // The even CTA's barriers in the cluster's shared window (its own, for the
+    // even CTA), computed once: a per-arrive branch on the CTA rank made the
+    // compiler spill while S is held in registers.
+    const uint32_t sfree_c = mapa(bar(B_SFREE), 0), ds_c = mapa(bar(B_DS), 0);
     bool ok = true;
     for (int jj = 0; jj < n_kv; ++jj) {
       const int k0 = (kr.x + jj) * 128 + 64 * h;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_S + (jj & 1)), (jj >> 1) & 1, lim));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DP), jj & 1, lim));
       if (!ok) break;
       tc_fence_after();
       uint32_t pf[64];
-      const uint32_t scol = (jj & 1) * 128 + 64 * h;
-      tmem_ld32(tmem + lane_base + scol, *reinterpret_cast<uint32_t(*)[32]>(&pf[0]));
-      tmem_ld32(tmem + lane_base + scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&pf[32]));
+      tmem_ld32(tmem + lane_base + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pf[0]));
+      tmem_ld32(tmem + lane_base + 32 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pf[32]));
       tmem_ld_wait();
+      tc_fence_before();
+      warp_arrive_cluster(sfree_c);  // S may be overwritten by S of tile jj+1
       const bool full = klo <= k0 && k0 + 63 <= khi;
       uint64_t pp[32];
 #pragma unroll
@@ -730,24 +743,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           pp[c] = f2(p0, p1);
         }
       }
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DP), jj & 1, lim));
-      if (!ok) break;
-      tc_fence_after();
-      // dP of key tile jj has completed, and with it dQ of tile jj-1: that
-      // tile's key stage is free for the producer.
-      if (warp == 0 && lane == 0 && jj > 0) mbar_arrive(bar(B_KEMPTY + (jj - 1) % NK));
-      __syncwarp();
+      const uint32_t dpb = tmem + lane_base + 128 + 128 * (jj & 1) + 64 * h;
       uint32_t dp[64];
-      tmem_ld32(tmem + lane_base + 256 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
-      tmem_ld32(tmem + lane_base + 288 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+      tmem_ld32(dpb, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+      tmem_ld32(dpb + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
       tmem_ld_wait();
       uint32_t dk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) dk[c] = f2_pack_bf16(f2_mul(pp[c], f2_sub(f2_bits(dp[2 * c], dp[2 * c + 1]), D2)));
-      tmem_st32(tmem + lane_base + 256 + 64 * h, dk);  // dS (bf16) over the dP columns this thread read
+      tmem_st32(dpb, dk);  // dS (bf16) over the dP columns this thread read
       tmem_st_wait();
       tc_fence_before();
-      warp_arrive_leader(bar(B_DS), crank);
+      warp_arrive_cluster(ds_c);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DONE), 0, lim));
     if (ok) {
@@ -801,57 +808,69 @@ struct PrepParams {
   float* rows[ULYSSES_MAX_P];
   int P, sl, bs, Hq, pitch;
   int fused, n;
-  long long rows_per_rank;  // sl * bs * Hq
 };
 
+// A block takes kPrepRows consecutive rows t of one (rank, batch, head): t is
+// the fastest index, so the LSE reads and the row-plane writes are
+// contiguous. Warp w takes rows [8w, 8w+8) of the block in four steps of two
+// rows, a half-warp (16 lanes x 16 bytes of O and of dO) per row, with all
+// eight loads of a lane issued before the first sum. grid.x covers t,
+// grid.y the (rank, batch, head) triples (strided past 65535).
+constexpr int kPrepRows = 64;
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constant__ PrepParams a) {
-  const long long total_rows = a.rows_per_rank * a.P;
-  const long long nthreads = (long long)gridDim.x * blockDim.x;
-  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  // The loop runs whole warps (the shuffle below needs every lane); lanes
-  // past the end add zeros.
-  const long long lane = threadIdx.x & 31;
-  for (long long g = tid; g - lane < total_rows * 16; g += nthreads) {
-    const bool active = g < total_rows * 16;
-    const long long row = active ? (g >> 4) : 0;
-    const int part = (int)(g & 15);
-    const int r = (int)(row / a.rows_per_rank);
-    const long long rr = row - (long long)r * a.rows_per_rank;  // (t, b, hq)
-    float acc = 0.f;
-    if (active) {
-      int src = r;
-      long long at = rr;  // row index (t, b, hq) within the source buffer
-      if (a.fused) {
-        const int hq = (int)(rr % a.Hq);
-        const long long tb = rr / a.Hq;
-        const long long t = tb / a.bs;
-        src = (int)(t / a.n);
-        at = ((tb - (long long)src * a.n * a.bs) * a.P + r) * a.Hq + hq;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int half = lane >> 4, part = lane & 15;
+  const int t0 = blockIdx.x * kPrepRows + warp * 8;
+  const long long triples = (long long)a.P * a.bs * a.Hq;
+  for (long long y = blockIdx.y; y < triples; y += gridDim.y) {
+    const int hq = (int)(y % a.Hq), b = (int)((y / a.Hq) % a.bs), r = (int)(y / ((long long)a.Hq * a.bs));
+    uint4 ov[4], dv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = t0 + 2 * u + half;
+      ov[u] = dv[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (t < a.sl) {
+        int src = r;
+        size_t at = ((size_t)t * a.bs + b) * a.Hq + hq;  // head shard: row (t, b, hq)
+        if (a.fused) {  // sequence shard t / n: row (t - s n, b, r Hq + hq)
+          src = t / a.n;
+          at = ((size_t)(t - src * a.n) * a.bs + b) * (size_t)(a.P * a.Hq) + (size_t)r * a.Hq + hq;
+        }
+        ov[u] = __ldg(reinterpret_cast<const uint4*>(a.o[src] + at * 128) + part);
+        dv[u] = __ldg(reinterpret_cast<const uint4*>(a.dO[src] + at * 128) + part);
       }
-      const uint4 ov = *reinterpret_cast<const uint4*>(a.o[src] + at * 128 + part * 8);
-      const uint4 dv = *reinterpret_cast<const uint4*>(a.dO[src] + at * 128 + part * 8);
-      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-      const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+    }
+    float acc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[u]);
+      const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv[u]);
+      float x = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 of = __bfloat1622float2(o2[e]);
         const float2 df = __bfloat1622float2(d2[e]);
-        acc = fmaf(of.x, df.x, fmaf(of.y, df.y, acc));
+        x = fmaf(of.x, df.x, fmaf(of.y, df.y, x));
       }
-    }
 #pragma unroll
-    for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (active && part < 2) {
-      const int hq = (int)(rr % a.Hq);
-      const long long tb = rr / a.Hq;
-      const int bb = (int)(tb % a.bs);
-      const long long t = tb / a.bs;
-      const long long plane = (long long)a.bs * a.Hq * a.pitch;
-      const long long at = ((long long)bb * a.Hq + hq) * a.pitch + t;
-      if (part == 0)
-        a.rows[r][plane + at] = acc;
-      else
-        a.rows[r][at] = -(a.lse[r][((long long)bb * a.Hq + hq) * a.sl + t] * 1.4426950408889634f);
+      for (int off = 8; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+      acc[u] = x;  // the sum of row 2u + half, in every lane of the half
+    }
+    // D of row j (0..7) to lane j: row j is step j/2 of half j%2.
+    float d = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float v0 = __shfl_sync(0xffffffffu, acc[u], 0), v1 = __shfl_sync(0xffffffffu, acc[u], 16);
+      if (lane == 2 * u) d = v0;
+      if (lane == 2 * u + 1) d = v1;
+    }
+    const size_t row = ((size_t)b * a.Hq + hq) * a.pitch + t0;
+    if (lane < 8) {
+      if (t0 + lane < a.sl) a.rows[r][(size_t)a.bs * a.Hq * a.pitch + row + lane] = d;
+    } else if (lane < 16) {
+      const int j = lane - 8;
+      if (t0 + j < a.sl)
+        a.rows[r][row + j] = -(a.lse[r][((size_t)b * a.Hq + hq) * a.sl + t0 + j] * 1.4426950408889634f);
     }
   }
 }
@@ -895,10 +914,6 @@ void plan_pair_tiles(const Layer& L, std::vector<int2>& kv_pairs, std::vector<in
 int64_t bwd_row_pitch(const Layer& L) { return (L.sl + 3) / 4 * 4; }
 size_t bwd_sm103_workspace(const Layer& L) { return (size_t)L.P * 2 * L.bs * L.Hq * bwd_row_pitch(L) * sizeof(float); }
 
-static int grid_cap(long long work) {
-  long long g = (work + 255) / 256;
-  return (int)std::max(1LL, std::min(g, 152LL * 16));
-}
 
 int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* const* k, const void* const* v,
                           const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,
@@ -936,9 +951,10 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
     a.pitch = (int)pitch;
     a.fused = fused ? 1 : 0;
     a.n = (int)L.n();
-    a.rows_per_rank = (long long)L.sl * L.bs * L.Hq;
     Timed t(L.timing, ULYSSES_KERNEL_BWD_PREP, stream);
-    attn_bwd_prep_kernel<<<grid_cap(a.rows_per_rank * L.P * 16), 256, 0, stream>>>(a);
+    const long long triples = (long long)L.P * L.bs * L.Hq;
+    const dim3 grid((unsigned)((L.sl + kPrepRows - 1) / kPrepRows), (unsigned)std::min(triples, 65535LL));
+    attn_bwd_prep_kernel<<<grid, 256, 0, stream>>>(a);
     t.done();
     count_launches(1);
   }

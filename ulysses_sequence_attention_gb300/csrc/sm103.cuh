@@ -307,6 +307,11 @@ __device__ __forceinline__ void warp_arrive_leader(uint32_t bar_local, uint32_t 
       mbar_arrive_cluster(mapa(bar_local, 0));
   }
 }
+// Per-warp arrival on a barrier given by its shared::cluster address.
+__device__ __forceinline__ void warp_arrive_cluster(uint32_t cluster_addr) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(cluster_addr);
+}
 __device__ __forceinline__ void warp_arrive_local(uint32_t bar_local) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar_local);
