@@ -118,7 +118,7 @@ enum {
   B_QFULL = 1,               // NQ: query-half part (Qn, dOn) landed (even CTA: + 1 forward)
   B_QEMPTY = B_QFULL + NQ,   // NQ: query-half part consumed by S^T, dP^T (1 compute thread, this CTA)
   B_HFULL = B_QEMPTY + NQ,   // NQ: head-half part (Qh, dOh) landed (even CTA: + 1 forward)
-  B_HEMPTY = B_HFULL + NQ,   // NQ: head-half part consumed by dV, dK (commit, both)
+  B_HEMPTY = B_HFULL + NQ,   // NQ: head-half part consumed by dV, dK (1 compute thread, this CTA)
   B_S = B_HEMPTY + NQ,       // S^T ready (commit, both)
   B_DP = B_S + 1,            // dP^T ready (commit, both)
   B_P = B_DP + 1,            // even CTA: P^T, dS^T written in both CTAs (16 warps)
@@ -212,46 +212,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tma_load_4d(sb + kOffV, &p.tb[l.map], bar(B_KV), 0, l.head, b, l.row);
         tma_load_4d(sb + kOffV + kHalf, &p.tb[l.map], bar(B_KV), 64, l.head, b, l.row);
       }
-      for (int it = 0; it < n_it; ++it) {
-        const int st = it % NQ, u = it / NQ;
-        const int hq = hk * p.group + it / nm;
-        const int m = qr.x + it % nm;
-        const uint32_t sq = sb + kOffStage + st * kStage;
-        const int q0 = m * 128;
-        // -LSE (log2 units) and D of the tile's 128 query rows, one TMA box
-        // from the two row planes. Rows past sl read as zero; every key masks
-        // them, so P = 0 there and dS = 0.
-        const int rsl = it % NR;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_REMPTY + rsl), ((it / NR) & 1) ^ 1, lim));
-        if (!ok) break;
-        if (lane == 0) {
-          mbar_expect_tx(bar(B_RFULL + rsl), 1024);
-          tma_load_3d(sb + kOffRow + rsl * 1024, &p.tr[rl], bar(B_RFULL + rsl), q0, b * p.Hq + hq, 0);
+      // The head part of tile it-1 is loaded after the query part of tile
+      // it: the compute warps free a head part only when they see the dP of
+      // the next tile complete (no commit of its own), so it is not needed
+      // before then.
+      for (int it = 0; it <= n_it; ++it) {
+        if (it < n_it) {
+          const int st = it % NQ, u = it / NQ;
+          const int hq = hk * p.group + it / nm;
+          const int q0 = (qr.x + it % nm) * 128;
+          const uint32_t sq = sb + kOffStage + st * kStage;
+          // -LSE (log2 units) and D of the tile's 128 query rows, one TMA box
+          // from the two row planes. Rows past sl read as zero; every key masks
+          // them, so P = 0 there and dS = 0.
+          const int rsl = it % NR;
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_REMPTY + rsl), ((it / NR) & 1) ^ 1, lim));
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_expect_tx(bar(B_RFULL + rsl), 1024);
+            tma_load_3d(sb + kOffRow + rsl * 1024, &p.tr[rl], bar(B_RFULL + rsl), q0, b * p.Hq + hq, 0);
+          }
+          n_r = it + 1;
+          // query-half part: Q and dO rows [q0 + 64c, +64) (B of S^T, dP^T: N = queries)
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QEMPTY + st), (u & 1) ^ 1, lim));
+          if (!ok) break;
+          if (lane == 0) {
+            const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hq, hq, q0);
+            const int qh = l.row + 64 * (int)crank;  // the tile's rows are in one shard
+            mbar_expect_tx(bar(B_QFULL + st), 2 * kHalf);
+            tma_load_4d(sq, &p.tc[l.map], bar(B_QFULL + st), 0, l.head, b, qh);
+            tma_load_4d(sq + kHalf / 2, &p.tc[l.map], bar(B_QFULL + st), 64, l.head, b, qh);
+            tma_load_4d(sq + kHalf, &p.td[l.map], bar(B_QFULL + st), 0, l.head, b, qh);
+            tma_load_4d(sq + kHalf + kHalf / 2, &p.td[l.map], bar(B_QFULL + st), 64, l.head, b, qh);
+          }
+          n_q = it + 1;
         }
-        n_r = it + 1;
-        // Both parts come from the same shard: the tile's rows are in one shard.
-        const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hq, hq, q0);
-        // query-half part: Q and dO rows [q0 + 64c, +64) (B of S^T, dP^T: N = queries)
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QEMPTY + st), (u & 1) ^ 1, lim));
-        if (!ok) break;
-        if (lane == 0) {
-          const int qh = l.row + 64 * (int)crank;
-          mbar_expect_tx(bar(B_QFULL + st), 2 * kHalf);
-          tma_load_4d(sq, &p.tc[l.map], bar(B_QFULL + st), 0, l.head, b, qh);
-          tma_load_4d(sq + kHalf / 2, &p.tc[l.map], bar(B_QFULL + st), 64, l.head, b, qh);
-          tma_load_4d(sq + kHalf, &p.td[l.map], bar(B_QFULL + st), 0, l.head, b, qh);
-          tma_load_4d(sq + kHalf + kHalf / 2, &p.td[l.map], bar(B_QFULL + st), 64, l.head, b, qh);
+        if (it >= 1) {
+          // head-half part of tile it-1: Q and dO columns [64c, 64c+64) of all 128 rows (B of dK, dV)
+          const int ih = it - 1, st = ih % NQ, u = ih / NQ;
+          const int hq = hk * p.group + ih / nm;
+          const int q0 = (qr.x + ih % nm) * 128;
+          const uint32_t sq = sb + kOffStage + st * kStage;
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_HEMPTY + st), (u & 1) ^ 1, lim));
+          if (!ok) break;
+          if (lane == 0) {
+            const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hq, hq, q0);
+            mbar_expect_tx(bar(B_HFULL + st), 2 * kHalf);
+            tma_load_4d(sq + 2 * kHalf, &p.te[l.map], bar(B_HFULL + st), 64 * (int)crank, l.head, b, l.row);
+            tma_load_4d(sq + 3 * kHalf, &p.tf[l.map], bar(B_HFULL + st), 64 * (int)crank, l.head, b, l.row);
+          }
+          n_h = ih + 1;
         }
-        n_q = it + 1;
-        // head-half part: Q and dO columns [64c, 64c+64) of all 128 rows (B of dK, dV)
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_HEMPTY + st), (u & 1) ^ 1, lim));
-        if (!ok) break;
-        if (lane == 0) {
-          mbar_expect_tx(bar(B_HFULL + st), 2 * kHalf);
-          tma_load_4d(sq + 2 * kHalf, &p.te[l.map], bar(B_HFULL + st), 64 * (int)crank, l.head, b, l.row);
-          tma_load_4d(sq + 3 * kHalf, &p.tf[l.map], bar(B_HFULL + st), 64 * (int)crank, l.head, b, l.row);
-        }
-        n_h = it + 1;
       }
       if (lane == 0) {
         if (!ok) pair_status(p);
@@ -326,7 +337,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             umma2_ts(tmem + 256, a, b_mn(sq + 3 * kHalf, kk), id_tm, acc);
             umma2_ts(tmem + 384, a + 32, b_mn(sq + 2 * kHalf, kk), id_tm, acc);
           }
-          umma2_commit_both(bar(B_HEMPTY + st));
           if (it + 1 < n_it) {
             issue_dp((it + 1) % NQ);  // its query part landed before S_{i+1} was issued
             umma2_commit_both(bar(B_DP));
@@ -358,12 +368,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         bool ok = mbar_wait(bar(B_KV), 0, lim);
         if (ok) mbar_arrive_cluster(mapa(bar(B_KV), 0));
-        for (int it = 0; it < n_it && ok; ++it) {
-          const int st = it % NQ, u = it / NQ;
-          ok = mbar_wait(bar(B_QFULL + st), u & 1, lim);
-          if (ok) mbar_arrive_cluster(mapa(bar(B_QFULL + st), 0));
-          if (ok) ok = mbar_wait(bar(B_HFULL + st), u & 1, lim);
-          if (ok) mbar_arrive_cluster(mapa(bar(B_HFULL + st), 0));
+        for (int it = 0; it <= n_it && ok; ++it) {  // in the producer's order
+          if (it < n_it) {
+            const int st = it % NQ, u = it / NQ;
+            ok = mbar_wait(bar(B_QFULL + st), u & 1, lim);
+            if (ok) mbar_arrive_cluster(mapa(bar(B_QFULL + st), 0));
+          }
+          if (ok && it >= 1) {
+            const int st = (it - 1) % NQ, u = (it - 1) / NQ;
+            ok = mbar_wait(bar(B_HFULL + st), u & 1, lim);
+            if (ok) mbar_arrive_cluster(mapa(bar(B_HFULL + st), 0));
+          }
         }
         if (!ok) pair_status(p);
       }
@@ -426,9 +441,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (warp == 0 && lane == 0) {
         // dP^T of tile it has completed, and with it S^T: the query part of
-        // its stage is free for the producer. (The head part is released by
-        // a commit right after dV/dK, which is earlier.)
+        // its stage is free for the producer. dV and dK of tile it-1 were
+        // issued before this dP, so they have completed too: the head part
+        // of that tile's stage is free.
         mbar_arrive(bar(B_QEMPTY + it % NQ));
+        if (it > 0) mbar_arrive(bar(B_HEMPTY + (it - 1) % NQ));
       }
       __syncwarp();
       uint32_t dp[64];
