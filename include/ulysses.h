@@ -366,6 +366,9 @@ int ulysses_set_wait_limit(ulysses_t h, int64_t cycles);
  *   kind 1: in the next tensor-core forward call, the TMA producer issues no
  *           K/V loads, so the waits for them run out. Combine with a short
  *           ulysses_set_wait_limit. The injection is consumed by that call.
+ *   kind 2: the same for the next tensor-core backward call: the dK/dV
+ *           kernel's producer issues no Q/dO tile loads. dK and dV are then
+ *           invalid; dQ is computed as usual.
  * Nothing faults, traps or hangs: every wait is bounded. Returns
  * ULYSSES_ERR_INVALID_ARG for an unknown kind. Host only.
  */

@@ -1,8 +1,9 @@
 """Failure detection on the GPU without a fault: a bounded wait that runs out.
 
-Every wait of the tensor-core kernels has a cycle limit. The test sets a short
-limit and injects a missing producer signal with the test hook
-(ulysses_inject_fault kind 1: no K/V loads are issued in the next forward).
+Every wait of the tensor-core kernels has a cycle limit. The tests set a short
+limit and inject a missing producer signal with the test hook
+(ulysses_inject_fault kind 1: no K/V loads are issued in the next forward;
+kind 2: no Q/dO loads in the next backward's dK/dV kernel).
 The consumers' waits then run out. The kernel sets the status word and
 returns, and ulysses_get_status reports ULYSSES_ERR_TIMEOUT. The same handle
 and CUDA context then compute a correct result. Nothing faults, traps or hangs.
@@ -56,3 +57,33 @@ def test_wait_limit_and_fault_kind_are_validated(u):
     with pytest.raises(u.UlyssesError):
         u.ulysses_inject_fault(h, 7)
     h.destroy()
+
+
+def test_backward_timeout_is_reported_and_the_context_survives(u):
+    """Kind 2: the next backward's dK/dV producer issues no Q/dO loads; its waits run out."""
+    sl, hc, hkv, P = 256, 2, 1, 1          # one CTA pair, two query tiles per query head
+    x = random_inputs(sl, 1, hc, hkv, 128, torch.bfloat16, 42)
+    L = u.UlyssesLayer(sl, 1, hc, hkv, 128, P, True, None, torch.bfloat16)
+    cu = lambda t: [s.cuda() for s in split_shards(t, P)]  # noqa: E731
+    q, k, v, do = cu(x["q"]), cu(x["k"]), cu(x["v"]), cu(x["do"])
+    o = L.new_seq_shards(hc)
+    dq, dk, dv = L.new_seq_shards(hc), L.new_seq_shards(hkv), L.new_seq_shards(hkv)
+    L.forward(q, k, v, o)
+    torch.cuda.synchronize()
+    assert u.ulysses_get_status(L.h) == u.ULYSSES_OK
+    u.ulysses_set_wait_limit(L.h, 200_000)
+    u.ulysses_inject_fault(L.h, 2)
+    L.backward(do, dq, dk, dv)
+    torch.cuda.synchronize()
+    assert u.ulysses_get_status(L.h) == u.ULYSSES_ERR_TIMEOUT
+    assert u.ulysses_get_status(L.h) == u.ULYSSES_OK
+    # consumed: the same handle, stream and context now give the right gradients
+    u.ulysses_set_wait_limit(L.h, 4_000_000_000)
+    L.backward(do, dq, dk, dv)
+    torch.cuda.synchronize()
+    assert u.ulysses_get_status(L.h) == u.ULYSSES_OK
+    qs, ks, vs, dos = (oracle.shard_sequence(x[n], P) for n in ("q", "k", "v", "do"))
+    g = oracle.ulysses_backward(qs, ks, vs, dos, P, causal=True)
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert_close(f"{name} after recovery", torch.cat([t.cpu() for t in got]), oracle.unshard_sequence(g[name]),
+                     torch.bfloat16)

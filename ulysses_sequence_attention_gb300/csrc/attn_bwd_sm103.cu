@@ -82,6 +82,7 @@ struct PairParams {
   int fused;                         // operands are sequence shards of n tokens (nranks = P)
   int n;
   int pitch;                         // floats per row of a row plane (sl rounded up to 4)
+  int skip_q_loads;                  // test hook (dK/dV): the producer issues no Q/dO tile loads
   float scale, scale_log2;
 };
 
@@ -236,7 +237,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // query-half part: Q and dO rows [q0 + 64c, +64) (B of S^T, dP^T: N = queries)
           ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QEMPTY + st), (u & 1) ^ 1, lim));
           if (!ok) break;
-          if (lane == 0) {
+          if (lane == 0 && !p.skip_q_loads) {
             const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hq, hq, q0);
             const int qh = l.row + 64 * (int)crank;  // the tile's rows are in one shard
             mbar_expect_tx(bar(B_QFULL + st), 2 * kHalf);
@@ -255,7 +256,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t sq = sb + kOffStage + st * kStage;
           ok = __all_sync(0xffffffffu, mbar_wait(bar(B_HEMPTY + st), (u & 1) ^ 1, lim));
           if (!ok) break;
-          if (lane == 0) {
+          if (lane == 0 && !p.skip_q_loads) {
             const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hq, hq, q0);
             mbar_expect_tx(bar(B_HFULL + st), 2 * kHalf);
             tma_load_4d(sq + 2 * kHalf, &p.te[l.map], bar(B_HFULL + st), 64 * (int)crank, l.head, b, l.row);
@@ -989,6 +990,9 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
   prm.pitch = (int)pitch;
   prm.fused = fused ? 1 : 0;
   prm.n = (int)L.n();
+  prm.skip_q_loads = 0;
+  const bool inject = L.inject_fault == 2;
+  if (inject) L.inject_fault = 0;
   prm.scale = (float)(1.0 / sqrt((double)L.hs));
   prm.scale_log2 = (float)(1.4426950408889634 / sqrt((double)L.hs));
   const int n_pair = (int)((L.sl + 255) / 256);
@@ -1002,6 +1006,7 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
     for (int r0 = 0; r0 < L.P; r0 += kRanksPerLaunch) {
       const int nr = std::min(kRanksPerLaunch, L.P - r0);
       prm.nranks = nr;
+      prm.skip_q_loads = (inject && pass == 0) ? 1 : 0;
       for (int i = 0; i < nr; ++i) {
         const int r = r0 + i;
         bool ok;

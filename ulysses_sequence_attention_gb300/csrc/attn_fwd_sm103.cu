@@ -451,7 +451,7 @@ int launch_attn_fwd_sm103(Layer& L, const void* const* q, const void* const* k, 
   prm.npairs = (group + 1) / 2;
   prm.causal = L.causal;
   prm.skip_kv_loads = L.inject_fault == 1 ? 1 : 0;
-  L.inject_fault = 0;
+  if (L.inject_fault == 1) L.inject_fault = 0;
   prm.scale_log2 = (float)(1.4426950408889634 / sqrt((double)L.hs));
   prm.fused = fused ? 1 : 0;
   prm.n = (int)L.n();

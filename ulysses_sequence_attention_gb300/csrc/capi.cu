@@ -362,7 +362,7 @@ int ulysses_set_wait_limit(ulysses_t h, int64_t cycles) {
 
 int ulysses_inject_fault(ulysses_t h, int kind) {
   Layer* L = reinterpret_cast<Layer*>(h);
-  if (!L || kind < 0 || kind > 1) return ULYSSES_ERR_INVALID_ARG;
+  if (!L || kind < 0 || kind > 2) return ULYSSES_ERR_INVALID_ARG;
   L->inject_fault = kind;
   return ULYSSES_OK;
 }

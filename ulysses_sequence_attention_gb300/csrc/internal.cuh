@@ -134,7 +134,7 @@ struct Layer {
   int2* d_qp_range = nullptr;
   int* d_qp_order = nullptr;
   long long timeout_cycles = 4000000000LL;  // bound of every device-side wait (~2 s)
-  int inject_fault = 0;                     // test hook (ulysses_inject_fault)
+  mutable int inject_fault = 0;             // test hook (ulysses_inject_fault), consumed by one call
   mutable Timing timing;                    // ulysses_timing_enable / ulysses_timing_read
   // Host-streaming steps (ulysses_host_begin / _step / _end): two copy
   // streams and, per device-buffer slot, the events that order its reuse.
