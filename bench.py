@@ -257,9 +257,7 @@ def run_ours(args, w, rank, world):
             return
         if timed:
             mark("fwd0")
-        B.ulysses_seq_to_head(h, w.hc, seq["q"], hb["qh"])
-        B.ulysses_seq_to_head(h, w.hkv, seq["k"], hb["kh"])
-        B.ulysses_seq_to_head(h, w.hkv, seq["v"], hb["vh"])
+        B.ulysses_seq_to_head_qkv(h, seq["q"], seq["k"], seq["v"], hb["qh"], hb["kh"], hb["vh"])
         B.ulysses_attn_fwd(h, hb["qh"], hb["kh"], hb["vh"], hb["oh"], lse)
         B.ulysses_head_to_seq(h, w.hc, hb["oh"], o)
         if timed:
@@ -268,26 +266,20 @@ def run_ours(args, w, rank, world):
             B.ulysses_seq_to_head(h, w.hc, seq["do"], hb["doh"])
             B.ulysses_attn_bwd(h, hb["qh"], hb["kh"], hb["vh"], hb["oh"], hb["doh"], lse,
                                hb["dqh"], hb["dkh"], hb["dvh"], ws)
-            B.ulysses_head_to_seq(h, w.hc, hb["dqh"], dq)
-            B.ulysses_head_to_seq(h, w.hkv, hb["dkh"], dk)
-            B.ulysses_head_to_seq(h, w.hkv, hb["dvh"], dv)
+            B.ulysses_head_to_seq_qkv(h, hb["dqh"], hb["dkh"], hb["dvh"], dq, dk, dv)
             if timed:
                 mark("bwd1")
 
     def exchange_step():
         """The explicit exchanges of one step: Q, K, V (and dO) seq->head, O (and dQ, dK, dV) head->seq."""
         mark("x0")
-        B.ulysses_seq_to_head(h, w.hc, seq["q"], hb["qh"])
-        B.ulysses_seq_to_head(h, w.hkv, seq["k"], hb["kh"])
-        B.ulysses_seq_to_head(h, w.hkv, seq["v"], hb["vh"])
+        B.ulysses_seq_to_head_qkv(h, seq["q"], seq["k"], seq["v"], hb["qh"], hb["kh"], hb["vh"])
         mark("x1")
         B.ulysses_head_to_seq(h, w.hc, hb["oh"], o)
         mark("x2")
         if w.backward:
             B.ulysses_seq_to_head(h, w.hc, seq["do"], hb["doh"])
-            B.ulysses_head_to_seq(h, w.hc, hb["dqh"], dq)
-            B.ulysses_head_to_seq(h, w.hkv, hb["dkh"], dk)
-            B.ulysses_head_to_seq(h, w.hkv, hb["dvh"], dv)
+            B.ulysses_head_to_seq_qkv(h, hb["dqh"], hb["dkh"], hb["dvh"], dq, dk, dv)
 
     def barrier():
         if world > 1:

@@ -195,6 +195,33 @@ int ulysses_head_to_seq(ulysses_t h, int nheads, const void* const* head_shards,
                         void* const* seq_shards, void* stream);
 
 /*
+ * ulysses_seq_to_head_qkv — the layer's first all-to-all for Q, K and V
+ * together, in one launch: the 3Nh message of the DeepSpeed-Ulysses blog,
+ * section "显著的通信量减少". Each tensor is exchanged exactly as
+ * ulysses_seq_to_head would (Q with hc heads, K and V with hkv heads, with kv
+ * replication when P > hkv). One launch covers all three, so the K and V
+ * exchanges, too small to fill the GPU on their own, share the Q
+ * exchange's waves.
+ *   q_seq, k_seq, v_seq     P sequence shards each (inputs)
+ *   q_head, k_head, v_head  P head shards each (outputs)
+ */
+int ulysses_seq_to_head_qkv(ulysses_t h, const void* const* q_seq, const void* const* k_seq,
+                            const void* const* v_seq, void* const* q_head, void* const* k_head,
+                            void* const* v_head, void* stream);
+
+/*
+ * ulysses_head_to_seq_qkv — the backward's last all-to-all for dQ, dK and dV
+ * together: ulysses_head_to_seq of each (dQ with hc heads, dK and dV with
+ * hkv heads), in one launch. When P > hkv the replica sums of dK and dV need
+ * their own kernel, and the three exchanges then run as three launches.
+ *   q_head, k_head, v_head  P head shards each (inputs: dQ, dK, dV)
+ *   q_seq, k_seq, v_seq     P sequence shards each (outputs)
+ */
+int ulysses_head_to_seq_qkv(ulysses_t h, const void* const* q_head, const void* const* k_head,
+                            const void* const* v_head, void* const* q_seq, void* const* k_seq,
+                            void* const* v_seq, void* stream);
+
+/*
  * ulysses_attn_fwd — local exact attention of every rank's head group.
  * HF blog algorithm step 4 (standard attention per head; heads are
  * independent). The DeepSpeed-Ulysses blog's per-head equation did not survive

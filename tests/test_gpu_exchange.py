@@ -133,3 +133,45 @@ def test_fullsize_exchanges_bit_exact(u, name):
             assert torch.equal(_bits(back[r].cpu()), _bits(seq[r]))
         del got, back
     h.destroy()
+
+
+@pytest.mark.parametrize("sl,bs,hc,hkv,hs,P,dtype", [
+    (1000, 2, 8, 2, 128, 2, torch.bfloat16),
+    (4096, 1, 32, 8, 128, 8, torch.bfloat16),
+    (96, 3, 12, 4, 64, 4, torch.float32),
+    (64, 2, 8, 2, 32, 8, torch.bfloat16),      # replicated kv heads (P > hkv)
+])
+def test_qkv_exchanges_in_one_call(u, sl, bs, hc, hkv, hs, P, dtype):
+    """ulysses_seq_to_head_qkv / ulysses_head_to_seq_qkv: each tensor as the single-tensor exchange, bit for bit."""
+    g = torch.Generator().manual_seed(sl * 3 + P)
+    h = u.ulysses_create(sl, bs, hc, hkv, hs, P, True, None, dtype)
+    xs = {"q": torch.randn((sl, bs, hc, hs), generator=g).to(dtype),
+          "k": torch.randn((sl, bs, hkv, hs), generator=g).to(dtype),
+          "v": torch.randn((sl, bs, hkv, hs), generator=g).to(dtype)}
+    seq = {k: oracle.shard_sequence(x, P) for k, x in xs.items()}
+    Hk = hkv // P if hkv % P == 0 else 1
+    heads = {"q": hc // P, "k": Hk, "v": Hk}
+    out = {k: [torch.full((sl, bs, heads[k], hs), float("nan"), dtype=dtype, device="cuda") for _ in range(P)]
+           for k in xs}
+    u.ulysses_seq_to_head_qkv(h, *[[s.cuda() for s in seq[k]] for k in ("q", "k", "v")],
+                              out["q"], out["k"], out["v"])
+    for k in xs:
+        want = oracle.seq_to_head(seq[k], P)
+        for r in range(P):
+            assert torch.equal(_bits(out[k][r].cpu()), _bits(want[r])), (k, r)
+    # head->seq of three gradients (summed over replicas when P > hkv)
+    grads = {k: [torch.randn((sl, bs, heads[k], hs), generator=g).to(dtype) for _ in range(P)] for k in xs}
+    back = {k: [torch.full((sl // P, bs, xs[k].shape[2], hs), float("nan"), dtype=dtype, device="cuda")
+                for _ in range(P)] for k in xs}
+    u.ulysses_head_to_seq_qkv(h, *[[t.cuda() for t in grads[k]] for k in ("q", "k", "v")],
+                              back["q"], back["k"], back["v"])
+    for k, H in (("q", hc), ("k", hkv), ("v", hkv)):
+        ref = _run_h2s(u, h, H, grads[k])        # the single-tensor exchange
+        for r in range(P):
+            assert torch.equal(_bits(back[k][r].cpu()), _bits(ref[r].cpu())), (k, r)
+    n0 = u.ulysses_launch_count()
+    u.ulysses_seq_to_head_qkv(h, *[[s.cuda() for s in seq[kk]] for kk in ("q", "k", "v")],
+                              out["q"], out["k"], out["v"])
+    assert u.ulysses_launch_count() - n0 == 1
+    torch.cuda.synchronize()
+    h.destroy()

@@ -26,10 +26,11 @@ def test_timing_counts_each_kernel_of_a_layer_step(fused):
     L.forward(q, k, v, o)              # not timed
     got = {name: u.ulysses_timing_read(L.h, i) for i, name in enumerate(u.KERNEL_NAMES)}
     # per step: one launch of each attention kernel; the explicit path adds
-    # seq->head of q, k, v, dO and head->seq of o, dq, dk, dv (the fused one
-    # reads and writes the sequence shards inside the attention kernels)
-    assert got["seq_to_head"][1] == (0 if fused else 2 * 4)
-    assert got["head_to_seq"][1] == (0 if fused else 2 * 4)
+    # seq->head of (q, k, v) and of dO, and head->seq of o and of (dq, dk, dv)
+    # (the fused one reads and writes the sequence shards inside the
+    # attention kernels)
+    assert got["seq_to_head"][1] == (0 if fused else 2 * 2)
+    assert got["head_to_seq"][1] == (0 if fused else 2 * 2)
     for name in ("attn_fwd", "bwd_prep", "bwd_dkdv", "bwd_dq"):
         assert got[name][1] == 2, name
     for name, (ms, n) in got.items():

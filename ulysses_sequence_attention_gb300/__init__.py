@@ -15,5 +15,6 @@ from ._binding import (  # noqa: F401
     ulysses_timing_enable, ulysses_timing_read, ULYSSES_KERNEL_COUNT, KERNEL_NAMES,
     ulysses_fused_supported, ulysses_layer_fwd, ulysses_layer_bwd,
     ulysses_host_begin, ulysses_host_step, ulysses_host_end, ulysses_create_varlen, ulysses_set_seq,
+    ulysses_seq_to_head_qkv, ulysses_head_to_seq_qkv,
 )
 from .layer import HostSteps, UlyssesLayer  # noqa: F401

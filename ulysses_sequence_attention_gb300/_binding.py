@@ -71,6 +71,10 @@ lib.ulysses_seq_to_head.argtypes = [_vp, ctypes.c_int, _pp, _pp, _vp]
 lib.ulysses_seq_to_head.restype = ctypes.c_int
 lib.ulysses_head_to_seq.argtypes = [_vp, ctypes.c_int, _pp, _pp, _vp]
 lib.ulysses_head_to_seq.restype = ctypes.c_int
+lib.ulysses_seq_to_head_qkv.argtypes = [_vp] + [_pp] * 6 + [_vp]
+lib.ulysses_seq_to_head_qkv.restype = ctypes.c_int
+lib.ulysses_head_to_seq_qkv.argtypes = [_vp] + [_pp] * 6 + [_vp]
+lib.ulysses_head_to_seq_qkv.restype = ctypes.c_int
 lib.ulysses_attn_fwd.argtypes = [_vp, _pp, _pp, _pp, _pp, _pp, _vp]
 lib.ulysses_attn_fwd.restype = ctypes.c_int
 lib.ulysses_attn_bwd.argtypes = [_vp] + [_pp] * 9 + [_vp, _vp]
@@ -248,6 +252,28 @@ def ulysses_head_to_seq(h: UlyssesHandle, nheads: int, head_shards, seq_shards, 
     src = _ptrs(h, head_shards, h.sl * h.bs * _heads_per_rank(h, nheads) * h.hs, dt, "head_shards")
     dst = _ptrs(h, seq_shards, n * h.bs * nheads * h.hs, dt, "seq_shards")
     _check(lib.ulysses_head_to_seq(h.ptr, int(nheads), src, dst, _stream(stream)), "ulysses_head_to_seq")
+
+
+def ulysses_seq_to_head_qkv(h: UlyssesHandle, q_seq, k_seq, v_seq, q_head, k_head, v_head, stream=None):
+    """seq->head of Q, K and V in one launch."""
+    dt = h.torch_dtype
+    n = h.sl // h.P
+    sq, sk = n * h.bs * h.hc * h.hs, n * h.bs * h.hkv * h.hs
+    hq, hk = h.sl * h.bs * h.Hq * h.hs, h.sl * h.bs * h.Hk * h.hs
+    args = [_ptrs(h, q_seq, sq, dt, "q_seq"), _ptrs(h, k_seq, sk, dt, "k_seq"), _ptrs(h, v_seq, sk, dt, "v_seq"),
+            _ptrs(h, q_head, hq, dt, "q_head"), _ptrs(h, k_head, hk, dt, "k_head"), _ptrs(h, v_head, hk, dt, "v_head")]
+    _check(lib.ulysses_seq_to_head_qkv(h.ptr, *args, _stream(stream)), "ulysses_seq_to_head_qkv")
+
+
+def ulysses_head_to_seq_qkv(h: UlyssesHandle, q_head, k_head, v_head, q_seq, k_seq, v_seq, stream=None):
+    """head->seq of dQ, dK and dV in one launch (three when kv heads are replicated)."""
+    dt = h.torch_dtype
+    n = h.sl // h.P
+    sq, sk = n * h.bs * h.hc * h.hs, n * h.bs * h.hkv * h.hs
+    hq, hk = h.sl * h.bs * h.Hq * h.hs, h.sl * h.bs * h.Hk * h.hs
+    args = [_ptrs(h, q_head, hq, dt, "q_head"), _ptrs(h, k_head, hk, dt, "k_head"), _ptrs(h, v_head, hk, dt, "v_head"),
+            _ptrs(h, q_seq, sq, dt, "q_seq"), _ptrs(h, k_seq, sk, dt, "k_seq"), _ptrs(h, v_seq, sk, dt, "v_seq")]
+    _check(lib.ulysses_head_to_seq_qkv(h.ptr, *args, _stream(stream)), "ulysses_head_to_seq_qkv")
 
 
 def ulysses_attn_fwd(h: UlyssesHandle, q, k, v, o, lse, stream=None):

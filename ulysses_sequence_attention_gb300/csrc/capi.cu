@@ -273,6 +273,42 @@ int ulysses_head_to_seq(ulysses_t h, int nheads, const void* const* head_shards,
   return uly::launch_head_to_seq(*L, nheads, head_shards, seq_shards, (cudaStream_t)stream);
 }
 
+int ulysses_seq_to_head_qkv(ulysses_t h, const void* const* q_seq, const void* const* k_seq,
+                            const void* const* v_seq, void* const* q_head, void* const* k_head, void* const* v_head,
+                            void* stream) {
+  const Layer* L = reinterpret_cast<const Layer*>(h);
+  if (!L) return ULYSSES_ERR_INVALID_ARG;
+  if (L->empty()) return ULYSSES_OK;
+  CHECK_PTRS(q_seq);
+  CHECK_PTRS(k_seq);
+  CHECK_PTRS(v_seq);
+  CHECK_PTRS(q_head);
+  CHECK_PTRS(k_head);
+  CHECK_PTRS(v_head);
+  const int nheads[3] = {L->hc, L->hkv, L->hkv};
+  const void* const* src[3] = {q_seq, k_seq, v_seq};
+  void* const* dst[3] = {q_head, k_head, v_head};
+  return uly::launch_seq_to_head_multi(*L, 3, nheads, src, dst, (cudaStream_t)stream);
+}
+
+int ulysses_head_to_seq_qkv(ulysses_t h, const void* const* q_head, const void* const* k_head,
+                            const void* const* v_head, void* const* q_seq, void* const* k_seq, void* const* v_seq,
+                            void* stream) {
+  const Layer* L = reinterpret_cast<const Layer*>(h);
+  if (!L) return ULYSSES_ERR_INVALID_ARG;
+  if (L->empty()) return ULYSSES_OK;
+  CHECK_PTRS(q_head);
+  CHECK_PTRS(k_head);
+  CHECK_PTRS(v_head);
+  CHECK_PTRS(q_seq);
+  CHECK_PTRS(k_seq);
+  CHECK_PTRS(v_seq);
+  const int nheads[3] = {L->hc, L->hkv, L->hkv};
+  const void* const* src[3] = {q_head, k_head, v_head};
+  void* const* dst[3] = {q_seq, k_seq, v_seq};
+  return uly::launch_head_to_seq_multi(*L, 3, nheads, src, dst, (cudaStream_t)stream);
+}
+
 int ulysses_attn_fwd(ulysses_t h, const void* const* q, const void* const* k,
                      const void* const* v, void* const* o, float* const* lse, void* stream) {
   Layer* L = reinterpret_cast<Layer*>(h);

@@ -53,6 +53,21 @@ struct S2HArgs {
   int H, P, replicated;
 };
 
+// Vector g of the destination (head shards) of one seq->head exchange: its
+// source address, and its destination in *out.
+__device__ __forceinline__ const uint4* s2h_vector(const S2HArgs& a, uint32_t g, uint4** out) {
+  uint32_t r, rem, row, v, t, b, s, tl;
+  a.per_rank.divmod(g, r, rem);
+  a.row_vecs.divmod(rem, row, v);
+  a.bs.divmod(row, t, b);
+  a.n.divmod(t, s, tl);
+  // First head of rank r's block (replicated: its single head r*H/P).
+  const uint32_t h0 = a.replicated ? (r * (uint32_t)a.H) / (uint32_t)a.P : r * a.row_vecs.d / a.head_vecs;
+  *out = reinterpret_cast<uint4*>(a.dst.p[r]) + rem;
+  return reinterpret_cast<const uint4*>(a.src.p[s]) + (size_t)(tl * a.bs.d + b) * a.src_row_vecs +
+         (size_t)h0 * a.head_vecs + v;
+}
+
 __global__ void __launch_bounds__(kThreads) seq_to_head_kernel(const __grid_constant__ S2HArgs a) {
   const uint32_t stride = gridDim.x * kThreads;
   for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < a.total; base += stride * kUnroll) {
@@ -62,18 +77,36 @@ __global__ void __launch_bounds__(kThreads) seq_to_head_kernel(const __grid_cons
     for (int u = 0; u < kUnroll; ++u) {
       const uint32_t g = base + u * stride;
       out[u] = nullptr;
-      if (g < a.total) {
-        uint32_t r, rem, row, v, t, b, s, tl;
-        a.per_rank.divmod(g, r, rem);
-        a.row_vecs.divmod(rem, row, v);
-        a.bs.divmod(row, t, b);
-        a.n.divmod(t, s, tl);
-        // First head of rank r's block (replicated: its single head r*H/P).
-        const uint32_t h0 = a.replicated ? (r * (uint32_t)a.H) / (uint32_t)a.P : r * a.row_vecs.d / a.head_vecs;
-        const uint4* src = reinterpret_cast<const uint4*>(a.src.p[s]) +
-                           (size_t)(tl * a.bs.d + b) * a.src_row_vecs + (size_t)h0 * a.head_vecs + v;
-        val[u] = __ldcs(src);
-        out[u] = reinterpret_cast<uint4*>(a.dst.p[r]) + rem;
+      if (g < a.total) val[u] = __ldcs(s2h_vector(a, g, &out[u]));
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (out[u]) *out[u] = val[u];
+  }
+}
+
+// Up to three exchanges in one launch (the layer's Q, K and V): the vector
+// index runs over the tensors one after the other, end[k] being the
+// cumulative vector count through tensor k.
+struct S2HMulti {
+  S2HArgs t[3];
+  uint32_t end[3];
+  int count;
+};
+
+__global__ void __launch_bounds__(kThreads) seq_to_head_multi_kernel(const __grid_constant__ S2HMulti m) {
+  const uint32_t total = m.end[m.count - 1];
+  const uint32_t stride = gridDim.x * kThreads;
+  for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < total; base += stride * kUnroll) {
+    uint4 val[kUnroll];
+    uint4* out[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t g = base + u * stride;
+      out[u] = nullptr;
+      if (g < total) {
+        const int k = g < m.end[0] ? 0 : (g < m.end[1] ? 1 : 2);
+        val[u] = __ldcs(s2h_vector(m.t[k], k ? g - m.end[k - 1] : g, &out[u]));
       }
     }
 #pragma unroll
@@ -93,6 +126,18 @@ struct H2SArgs {
   uint32_t n;          // tokens per sequence shard
 };
 
+// Vector g of the destination (sequence shards) of one head->seq exchange.
+__device__ __forceinline__ const uint4* h2s_vector(const H2SArgs& a, uint32_t g, uint4** out) {
+  uint32_t s, rem, row, v, tl, b, r, w;
+  a.per_shard.divmod(g, s, rem);
+  a.row_vecs.divmod(rem, row, v);
+  a.bs.divmod(row, tl, b);
+  a.block_vecs.divmod(v, r, w);
+  const uint32_t t = s * a.n + tl;
+  *out = reinterpret_cast<uint4*>(a.dst.p[s]) + rem;
+  return reinterpret_cast<const uint4*>(a.src.p[r]) + (size_t)(t * a.bs.d + b) * a.block_vecs.d + w;
+}
+
 __global__ void __launch_bounds__(kThreads) head_to_seq_kernel(const __grid_constant__ H2SArgs a) {
   const uint32_t stride = gridDim.x * kThreads;
   for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < a.total; base += stride * kUnroll) {
@@ -102,17 +147,34 @@ __global__ void __launch_bounds__(kThreads) head_to_seq_kernel(const __grid_cons
     for (int u = 0; u < kUnroll; ++u) {
       const uint32_t g = base + u * stride;
       out[u] = nullptr;
-      if (g < a.total) {
-        uint32_t s, rem, row, v, tl, b, r, w;
-        a.per_shard.divmod(g, s, rem);
-        a.row_vecs.divmod(rem, row, v);
-        a.bs.divmod(row, tl, b);
-        a.block_vecs.divmod(v, r, w);
-        const uint32_t t = s * a.n + tl;
-        const uint4* src = reinterpret_cast<const uint4*>(a.src.p[r]) +
-                           (size_t)(t * a.bs.d + b) * a.block_vecs.d + w;
-        val[u] = __ldcs(src);
-        out[u] = reinterpret_cast<uint4*>(a.dst.p[s]) + rem;
+      if (g < a.total) val[u] = __ldcs(h2s_vector(a, g, &out[u]));
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (out[u]) *out[u] = val[u];
+  }
+}
+
+// Up to three head->seq exchanges in one launch (dQ, dK and dV).
+struct H2SMulti {
+  H2SArgs t[3];
+  uint32_t end[3];
+  int count;
+};
+
+__global__ void __launch_bounds__(kThreads) head_to_seq_multi_kernel(const __grid_constant__ H2SMulti m) {
+  const uint32_t total = m.end[m.count - 1];
+  const uint32_t stride = gridDim.x * kThreads;
+  for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < total; base += stride * kUnroll) {
+    uint4 val[kUnroll];
+    uint4* out[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t g = base + u * stride;
+      out[u] = nullptr;
+      if (g < total) {
+        const int k = g < m.end[0] ? 0 : (g < m.end[1] ? 1 : 2);
+        val[u] = __ldcs(h2s_vector(m.t[k], k ? g - m.end[k - 1] : g, &out[u]));
       }
     }
 #pragma unroll
@@ -154,21 +216,21 @@ int grid_for(uint64_t items_per_thread_block) {
 
 }  // namespace
 
-int launch_seq_to_head(const Layer& L, int nheads, const void* const* src, void* const* dst,
-                       cudaStream_t stream) {
+// Arguments of one seq->head exchange of an nheads-head tensor; its vector count in *total.
+static int make_s2h(const Layer& L, int nheads, const void* const* src, void* const* dst, S2HArgs& a,
+                    uint64_t* total) {
   const int H = nheads;
   const bool replicated = (H % L.P) != 0;
   const int Hh = replicated ? 1 : H / L.P;
   const uint32_t head_vecs = (uint32_t)(L.hs * L.esize() / 16);
   const uint64_t per_rank = (uint64_t)L.sl * L.bs * Hh * head_vecs;
-  const uint64_t total = per_rank * L.P;
-  if (total >= (1ull << 32)) return ULYSSES_ERR_UNSUPPORTED;
-  S2HArgs a;
+  *total = per_rank * L.P;
+  if (*total >= (1ull << 32)) return ULYSSES_ERR_UNSUPPORTED;
   for (int r = 0; r < L.P; ++r) {
     a.src.p[r] = src[r];
     a.dst.p[r] = dst[r];
   }
-  a.total = (uint32_t)total;
+  a.total = (uint32_t)*total;
   a.per_rank = FastDiv((uint32_t)per_rank);
   a.row_vecs = FastDiv((uint32_t)Hh * head_vecs);
   a.bs = FastDiv((uint32_t)L.bs);
@@ -178,8 +240,60 @@ int launch_seq_to_head(const Layer& L, int nheads, const void* const* src, void*
   a.H = H;
   a.P = L.P;
   a.replicated = replicated ? 1 : 0;
+  return ULYSSES_OK;
+}
+
+// Arguments of one head->seq exchange (nheads % P == 0); its vector count in *total.
+static int make_h2s(const Layer& L, int nheads, const void* const* src, void* const* dst, H2SArgs& a,
+                    uint64_t* total) {
+  const int H = nheads;
+  const uint64_t n = (uint64_t)L.n();
+  const int Hh = H / L.P;
+  const uint32_t head_vecs = (uint32_t)(L.hs * L.esize() / 16);
+  const uint64_t per_shard = n * L.bs * H * head_vecs;
+  *total = per_shard * L.P;
+  if (*total >= (1ull << 32)) return ULYSSES_ERR_UNSUPPORTED;
+  for (int r = 0; r < L.P; ++r) {
+    a.src.p[r] = src[r];
+    a.dst.p[r] = dst[r];
+  }
+  a.total = (uint32_t)*total;
+  a.per_shard = FastDiv((uint32_t)per_shard);
+  a.row_vecs = FastDiv((uint32_t)H * head_vecs);
+  a.bs = FastDiv((uint32_t)L.bs);
+  a.block_vecs = FastDiv((uint32_t)Hh * head_vecs);
+  a.n = (uint32_t)n;
+  return ULYSSES_OK;
+}
+
+int launch_seq_to_head(const Layer& L, int nheads, const void* const* src, void* const* dst,
+                       cudaStream_t stream) {
+  S2HArgs a;
+  uint64_t total = 0;
+  const int st = make_s2h(L, nheads, src, dst, a, &total);
+  if (st != ULYSSES_OK) return st;
   Timed t(L.timing, ULYSSES_KERNEL_SEQ_TO_HEAD, stream);
   seq_to_head_kernel<<<grid_for(total), kThreads, 0, stream>>>(a);
+  t.done();
+  count_launches(1);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_seq_to_head_multi(const Layer& L, int count, const int* nheads, const void* const* const* src,
+                             void* const* const* dst, cudaStream_t stream) {
+  S2HMulti m;
+  uint64_t end = 0;
+  m.count = count;
+  for (int k = 0; k < count; ++k) {
+    uint64_t total = 0;
+    const int st = make_s2h(L, nheads[k], src[k], dst[k], m.t[k], &total);
+    if (st != ULYSSES_OK) return st;
+    end += total;
+    if (end >= (1ull << 32)) return ULYSSES_ERR_UNSUPPORTED;
+    m.end[k] = (uint32_t)end;
+  }
+  Timed t(L.timing, ULYSSES_KERNEL_SEQ_TO_HEAD, stream);
+  seq_to_head_multi_kernel<<<grid_for(end), kThreads, 0, stream>>>(m);
   t.done();
   count_launches(1);
   return cuda_status(cudaGetLastError());
@@ -216,24 +330,41 @@ int launch_head_to_seq(const Layer& L, int nheads, const void* const* src, void*
     count_launches(1);
     return cuda_status(cudaGetLastError());
   }
-  const int Hh = H / L.P;
-  const uint32_t head_vecs = (uint32_t)(L.hs * L.esize() / 16);
-  const uint64_t per_shard = n * L.bs * H * head_vecs;
-  const uint64_t total = per_shard * L.P;
-  if (total >= (1ull << 32)) return ULYSSES_ERR_UNSUPPORTED;
   H2SArgs a;
-  for (int r = 0; r < L.P; ++r) {
-    a.src.p[r] = src[r];
-    a.dst.p[r] = dst[r];
-  }
-  a.total = (uint32_t)total;
-  a.per_shard = FastDiv((uint32_t)per_shard);
-  a.row_vecs = FastDiv((uint32_t)H * head_vecs);
-  a.bs = FastDiv((uint32_t)L.bs);
-  a.block_vecs = FastDiv((uint32_t)Hh * head_vecs);
-  a.n = (uint32_t)n;
+  uint64_t total = 0;
+  const int st = make_h2s(L, H, src, dst, a, &total);
+  if (st != ULYSSES_OK) return st;
   Timed t(L.timing, ULYSSES_KERNEL_HEAD_TO_SEQ, stream);
   head_to_seq_kernel<<<grid_for(total), kThreads, 0, stream>>>(a);
+  t.done();
+  count_launches(1);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_head_to_seq_multi(const Layer& L, int count, const int* nheads, const void* const* const* src,
+                             void* const* const* dst, cudaStream_t stream) {
+  for (int k = 0; k < count; ++k)
+    if (nheads[k] % L.P != 0) {
+      // Replicated kv heads need the replica sum: one launch per tensor.
+      for (int j = 0; j < count; ++j) {
+        const int st = launch_head_to_seq(L, nheads[j], src[j], dst[j], stream);
+        if (st != ULYSSES_OK) return st;
+      }
+      return ULYSSES_OK;
+    }
+  H2SMulti m;
+  uint64_t end = 0;
+  m.count = count;
+  for (int k = 0; k < count; ++k) {
+    uint64_t total = 0;
+    const int st = make_h2s(L, nheads[k], src[k], dst[k], m.t[k], &total);
+    if (st != ULYSSES_OK) return st;
+    end += total;
+    if (end >= (1ull << 32)) return ULYSSES_ERR_UNSUPPORTED;
+    m.end[k] = (uint32_t)end;
+  }
+  Timed t(L.timing, ULYSSES_KERNEL_HEAD_TO_SEQ, stream);
+  head_to_seq_multi_kernel<<<grid_for(end), kThreads, 0, stream>>>(m);
   t.done();
   count_launches(1);
   return cuda_status(cudaGetLastError());

@@ -182,6 +182,12 @@ int launch_seq_to_head(const Layer& L, int nheads, const void* const* src, void*
                        cudaStream_t s);
 int launch_head_to_seq(const Layer& L, int nheads, const void* const* src, void* const* dst,
                        cudaStream_t s);
+// count (<= 3) exchanges in one launch: tensor k has nheads[k] heads, P source
+// pointers src[k] and P destination pointers dst[k].
+int launch_seq_to_head_multi(const Layer& L, int count, const int* nheads, const void* const* const* src,
+                             void* const* const* dst, cudaStream_t s);
+int launch_head_to_seq_multi(const Layer& L, int count, const int* nheads, const void* const* const* src,
+                             void* const* const* dst, cudaStream_t s);
 int launch_attn_fwd_simt(const Layer& L, const void* const* q, const void* const* k,
                          const void* const* v, void* const* o, float* const* lse, cudaStream_t s);
 int launch_attn_bwd_simt(const Layer& L, const void* const* q, const void* const* k,

@@ -120,9 +120,7 @@ class UlyssesLayer:
             B.ulysses_layer_fwd(self.h, q_seq, k_seq, v_seq, o_seq, b["lse"], stream)
             self._saved = (q_seq, k_seq, v_seq, o_seq)
             return o_seq
-        B.ulysses_seq_to_head(self.h, self.hc, q_seq, b["qh"], stream)
-        B.ulysses_seq_to_head(self.h, self.hkv, k_seq, b["kh"], stream)
-        B.ulysses_seq_to_head(self.h, self.hkv, v_seq, b["vh"], stream)
+        B.ulysses_seq_to_head_qkv(self.h, q_seq, k_seq, v_seq, b["qh"], b["kh"], b["vh"], stream)
         B.ulysses_attn_fwd(self.h, b["qh"], b["kh"], b["vh"], b["oh"], b["lse"], stream)
         B.ulysses_head_to_seq(self.h, self.hc, b["oh"], o_seq, stream)
         return o_seq
@@ -139,9 +137,7 @@ class UlyssesLayer:
         B.ulysses_seq_to_head(self.h, self.hc, do_seq, b["doh"], stream)
         B.ulysses_attn_bwd(self.h, b["qh"], b["kh"], b["vh"], b["oh"], b["doh"], b["lse"],
                            b["dqh"], b["dkh"], b["dvh"], b["ws"], stream)
-        B.ulysses_head_to_seq(self.h, self.hc, b["dqh"], dq_seq, stream)
-        B.ulysses_head_to_seq(self.h, self.hkv, b["dkh"], dk_seq, stream)
-        B.ulysses_head_to_seq(self.h, self.hkv, b["dvh"], dv_seq, stream)
+        B.ulysses_head_to_seq_qkv(self.h, b["dqh"], b["dkh"], b["dvh"], dq_seq, dk_seq, dv_seq, stream)
         return dq_seq, dk_seq, dv_seq
 
     @property
