@@ -495,7 +495,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tma_store_4d(&p.tg[l.map], sb + kOffK, 0, l.head, b, l.row);
           tma_store_4d(&p.tg[l.map], sb + kOffK + kHalf, 64, l.head, b, l.row);
           bulk_commit();
-          bulk_wait_all();
+          bulk_wait_read_all();  // the stores have read shared memory; their global writes complete before the grid does
         } else {
           pair_status(p);
         }
@@ -795,7 +795,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tma_store_4d(&p.tf[l.map], sb + kOffQ, 0, l.head, b, l.row);
           tma_store_4d(&p.tf[l.map], sb + kOffQ + kHalf, 64, l.head, b, l.row);
           bulk_commit();
-          bulk_wait_all();
+          bulk_wait_read_all();  // the stores have read shared memory; their global writes complete before the grid does
         } else {
           pair_status(p);
         }

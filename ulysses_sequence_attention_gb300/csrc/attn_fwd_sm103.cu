@@ -396,7 +396,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_store_4d(&p.to[lo_.map], stage, 0, lo_.head, b, lo_.row);
             tma_store_4d(&p.to[lo_.map], stage + kHalf, 64, lo_.head, b, lo_.row);
             bulk_commit();
-            bulk_wait_all();
+            bulk_wait_read_all();  // the stores have read shared memory; their global writes complete before the grid does
           } else {
             atomicOr(p.status, STATUS_TIMEOUT);
           }
