@@ -937,15 +937,15 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
                           const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,
                           void* const* dk, void* const* dv, void* workspace, cudaStream_t stream, bool fused) {
   if (fused && !fused_supported(L)) return ULYSSES_ERR_UNSUPPORTED;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dkdv::kSmem) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dqk::kSmem) !=
-            cudaSuccess)
-      return ULYSSES_ERR_CUDA;
-    attr_set = true;
-  }
+  static PerDeviceOnce attrs;
+  const int ast = attrs.run([] {
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dkdv::kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dqk::kSmem);
+    return e;
+  });
+  if (ast != ULYSSES_OK) return ast;
   // Workspace: per rank two row planes, -LSE*log2(e) then D, each
   // [bs*Hq][pitch] fp32 with the pitch a multiple of 16 bytes (a TMA stride).
   float* ws = reinterpret_cast<float*>(workspace);

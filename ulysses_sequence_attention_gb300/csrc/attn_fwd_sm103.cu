@@ -427,13 +427,11 @@ bool fused_supported(const Layer& L) {
 
 int launch_attn_fwd_sm103(Layer& L, const void* const* q, const void* const* k, const void* const* v,
                           void* const* o, float* const* lse, cudaStream_t stream, bool fused) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(attn_fwd_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-        cudaSuccess)
-      return ULYSSES_ERR_CUDA;
-    attr_set = true;
-  }
+  static PerDeviceOnce attrs;
+  const int st = attrs.run([] {
+    return cudaFuncSetAttribute(attn_fwd_sm103_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  });
+  if (st != ULYSSES_OK) return st;
   const int n_pair = (int)((L.sl + 255) / 256);
   const int group = L.Hq / L.Hk;
   FwdParams prm;

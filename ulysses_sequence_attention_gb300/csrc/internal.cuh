@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
+#include <atomic>
 #include <vector>
 
 #include "../../include/ulysses.h"
@@ -218,6 +219,23 @@ inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? ULYSSES_OK : U
 
 // Adds n to the library-wide kernel launch counter (ulysses_launch_count).
 void count_launches(int n);
+
+// Runs a configuration step (kernel attributes) once per device: function
+// attributes are per device, so a process that drives several GPUs needs it
+// on each. Setting an attribute twice (two host threads racing) is harmless.
+struct PerDeviceOnce {
+  std::atomic<uint64_t> done{0};  // bit d: device d configured (devices >= 64: every call)
+  template <class F>
+  int run(F&& configure) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ULYSSES_ERR_CUDA;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return ULYSSES_OK;
+    if (configure() != cudaSuccess) return ULYSSES_ERR_CUDA;
+    if (bit) done.fetch_or(bit, std::memory_order_release);
+    return ULYSSES_OK;
+  }
+};
 
 // Frees the host-streaming streams and events of a handle (host_step.cu).
 void destroy_host_pipe(Layer& L);
