@@ -46,21 +46,6 @@ inline bool make_tmap_bf16_4d(CUtensorMap* map, const void* base, uint64_t d0, u
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The same for an fp32 tensor (the dQ accumulator). With 128-byte swizzle the
-// box is 32 floats wide.
-inline bool make_tmap_f32_4d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3,
-                             uint32_t box0, uint32_t box3, CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
-  EncodeTiledFn fn = encode_tiled_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[4] = {d0, d1, d2, d3};
-  const cuuint64_t strides[3] = {d0 * 4, d0 * d1 * 4, d0 * d1 * d2 * 4};
-  const cuuint32_t box[4] = {box0, 1, 1, box3};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // The two fp32 row planes of the backward, [2][nrows][pitch] (pitch a
 // multiple of 4 floats; only the first `len` floats of a row are in the
 // tensor, so reads past them return zero), in boxes of 128 x 1 x 2: the same
@@ -74,20 +59,6 @@ inline bool make_tmap_f32_rows(CUtensorMap* map, const void* base, uint64_t len,
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// A rank-2 bf16 tensor [d1][d0], boxes of box0 x box1, 128-byte swizzle.
-inline bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint32_t box0,
-                              uint32_t box1) {
-  EncodeTiledFn fn = encode_tiled_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {d0, d1};
-  const cuuint64_t strides[1] = {d0 * 2};
-  const cuuint32_t box[2] = {box0, box1};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
