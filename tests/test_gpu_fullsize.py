@@ -156,3 +156,15 @@ def test_alst_128k_spot_check(u):
     rng = np.random.default_rng(87)
     tail = torch.tensor(np.sort(rng.choice(np.arange(w.sl - 512, w.sl), 16, replace=False)))
     check_cols(w, x, got, kv_heads=[0, 7], cols=tail)
+
+
+@pytest.mark.slow
+def test_alst_512k_spot_check(u):
+    """The 512K-token layer (context for the pages' 500K-token ALST run): sampled rows and tail keys."""
+    w = WORKLOADS["alst_512k"]
+    x = make_global_inputs(w)
+    got = run_workload(u, w, x)
+    check_rows(w, x, got, heads=range(0, w.hc, 4), rows_per_head=16, seed=88)
+    rng = np.random.default_rng(89)
+    tail = torch.tensor(np.sort(rng.choice(np.arange(w.sl - 512, w.sl), 8, replace=False)))
+    check_cols(w, x, got, kv_heads=[3], cols=tail)

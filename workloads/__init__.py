@@ -72,6 +72,11 @@ WORKLOADS = {
     # Packed batch of 16 documents, per-document causal, forward + backward.
     "packed_64k": Workload("packed_64k", P=8, bs=1, sl=65536, hc=32, hkv=8, hs=128,
                            dtype="bf16", causal=True, seed=4, backward=True, ndoc=16),
+    # Context for the pages' ALST figure (a 500K-token Llama-8B sequence trained
+    # on one H100): the attention layer of a 512K-token sequence, forward +
+    # backward, on one GPU.
+    "alst_512k": Workload("alst_512k", P=8, bs=1, sl=524288, hc=32, hkv=8, hs=128,
+                          dtype="bf16", causal=True, seed=5, backward=True),
 }
 
 
