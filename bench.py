@@ -78,28 +78,34 @@ def exchange_bytes(w, H):
 KERNEL_SOURCES = {
     "attn_bwd_dkdv_kernel": "ulysses_sequence_attention_gb300/csrc/attn_bwd_sm103.cu",
     "attn_bwd_dq_kernel": "ulysses_sequence_attention_gb300/csrc/attn_bwd_sm103.cu",
+    "attn_bwd_dq_stored_kernel": "ulysses_sequence_attention_gb300/csrc/attn_bwd_sm103.cu",
     "attn_fwd_sm103_kernel": "ulysses_sequence_attention_gb300/csrc/attn_fwd_sm103.cu",
 }
 
 
-def kernel_work(w, offs):
+def kernel_work(w, offs, ds_bytes=0):
     """Per timed kernel id: (CUDA kernel name, bound, algorithmic work of one step, unit).
 
     Tensor kernels count 2*hs flops per visible (query, key) pair, head and
     GEMM. The forward needs 2 GEMMs (S = Q K^T, O = P V). The dK/dV kernel
     needs 4 (S, dP = dO V^T, dV = P^T dO, dK = dS^T Q), none of them repeated
-    inside it. The dQ kernel issues 3 (S, dP, dQ = dS K), of which S and dP
-    repeat the dK/dV kernel's: its algorithmic share of the 5-GEMM backward
-    is the dQ GEMM alone. Byte-bound kernels count one read and one write of
-    what they move.
+    inside it. The recomputing dQ kernel issues 3 (S, dP, dQ = dS K), of which
+    S and dP repeat the dK/dV kernel's: its algorithmic share of the 5-GEMM
+    backward is the dQ GEMM alone. With stored dS (ds_bytes > 0: the area's
+    blocks, zero block excluded) the dQ kernel is one GEMM at 128 flops per
+    byte of dS, below the machine balance: it is counted as byte-bound, one
+    read of every stored block, of K and one write of dQ. Byte-bound kernels
+    count one read and one write of what they move.
     """
     fl2 = attn_flops(w, offs=offs) / 2.0   # one GEMM over the visible pairs
     tok = w.sl * w.bs
     eb = w.elem_bytes
+    dq = (("attn_bwd_dq_stored_kernel", "hbm", ds_bytes + tok * (w.hc + w.hkv) * w.hs * eb, "byte") if ds_bytes
+          else ("attn_bwd_dq_kernel", "tensor", 1 * fl2, "flop"))
     return {
         "attn_fwd": ("attn_fwd_sm103_kernel", "tensor", 2 * fl2, "flop"),
         "bwd_dkdv": ("attn_bwd_dkdv_kernel", "tensor", 4 * fl2, "flop"),
-        "bwd_dq": ("attn_bwd_dq_kernel", "tensor", 1 * fl2, "flop"),
+        "bwd_dq": dq,
         "bwd_prep": ("attn_bwd_prep_kernel", "hbm", tok * w.hc * (2 * w.hs * eb + 4), "byte"),
         "seq_to_head": ("seq_to_head_kernel", "hbm",
                         exchange_bytes(w, w.hc) * (2 if w.backward else 1) + 2 * exchange_bytes(w, w.hkv), "byte"),
@@ -218,7 +224,7 @@ def run_ours(args, w, rank, world):
     seq = {k: [t.to(dev) for t in split_shards(v, P)] for k, v in x.items()}
     fused = None if args.path == "auto" else args.path == "fused"
     L = U.UlyssesLayer(w.sl, w.bs, w.hc, w.hkv, w.hs, P, w.causal, offs, w.torch_dtype, device=str(dev),
-                       fused=fused)
+                       fused=fused, ds_budget=args.ds_budget)
     o = L.new_seq_shards(w.hc)
     if w.backward:
         dq, dk, dv = L.new_seq_shards(w.hc), L.new_seq_shards(w.hkv), L.new_seq_shards(w.hkv)
@@ -356,7 +362,8 @@ def run_ours(args, w, rank, world):
 
     result = {"ms_per_step": ms_per_step, "value": value, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
               "s2h_qkv_ms": s2h_ms, "h2s_o_ms": h2s_ms, "launches": launches, "clocks": clk, "e2e": e2e,
-              "kernels": kernels, "path": "fused" if L.fused else "explicit"}
+              "kernels": kernels, "path": "fused" if L.fused else "explicit",
+              "ds_bytes": B.ulysses_ds_bytes(h)}
     return result
 
 
@@ -509,6 +516,8 @@ def main():
                     help="fused: exchanges inside the attention kernels (where the shape allows); "
                          "explicit: exchange kernels between the attention calls")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ds-budget", type=int, default=None,
+                    help="bytes the backward may keep dS in (default: the layer's; 0 recomputes dQ)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sl", type=int, default=4096, help="oracle sample length for cpu_baseline")
     ap.add_argument("--ref-sl", type=int, default=1024, help="oracle sample length per reference step")
@@ -552,7 +561,8 @@ def main():
         s2h_gbs = x_bytes / (r["s2h_qkv_ms"] * 1e-3) / 1e9
         h2s_gbs = exchange_bytes(w, w.hc) / (r["h2s_o_ms"] * 1e-3) / 1e9
         sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-        work = kernel_work(w, offs)
+        ds_blocks = max(r["ds_bytes"] - 32768, 0)   # the stored blocks, zero block excluded
+        work = kernel_work(w, offs, ds_blocks)
         per_kernel = {}
         for name, k in r["kernels"].items():
             cname, bound, units, unit = work[name]
@@ -561,7 +571,7 @@ def main():
                                     **({"tflops": rate / 1e12, "frac_sustained": rate / 1e12 / sustained}
                                        if unit == "flop" else
                                        {"gbs": rate / 1e9, "frac_hbm": rate / 1e9 / peaks["hbm_gbs"]}))
-            if name == "bwd_dq":   # S and dP are issued again here: 3 GEMMs run, 1 is its own
+            if name == "bwd_dq" and not ds_blocks:   # S and dP are issued again here: 3 GEMMs run, 1 is its own
                 per_kernel[name]["issued_tflops"] = 3 * rate / 1e12
         # the dominant kernel: the largest share of the timed step's device time
         top = max((n for n in r["kernels"] if "region" not in r["kernels"][n]),
@@ -602,6 +612,9 @@ def main():
                 "kernels": per_kernel,
                 "clocks": r["clocks"],
                 "path": r["path"],
+                "backward_dq": ({"how": "stored dS: the dK/dV kernel writes bf16 dS, dQ = s dS K reads it back",
+                                 "ds_bytes": r["ds_bytes"]} if ds_blocks else
+                                {"how": "recomputed: the dQ kernel forms S, P, dP and dS again"}),
                 "attention": {"fwd_ms": attn_fwd_ms, "fwd_tflops": fwd_tf, "fwd_frac_sustained": fwd_tf / sustained,
                               "bwd_ms": attn_bwd_ms, "bwd_tflops": bwd_tf,
                               "bwd_frac_sustained": (bwd_tf / sustained) if bwd_tf else None,

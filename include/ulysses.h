@@ -157,10 +157,46 @@ const char* ulysses_strerror(int status);
  * bf16 with hs = 128 (the tensor-core path): for each rank, two fp32 row
  * planes [bs][hc/P][pitch], -LSE*log2(e) and D = rowsum(dO * O), where pitch
  * is sl rounded up to a multiple of 4: P * 2 * bs * (hc/P) * pitch * 4 bytes.
- * Other configurations: D only, P * bs * (hc/P) * sl * 4 bytes. Pure host
+ * Other configurations: D only, P * bs * (hc/P) * sl * 4 bytes. With stored
+ * dS on (ulysses_set_ds_budget), add the stored-dS area after the row planes
+ * (at an offset rounded up to 1024 bytes): ulysses_ds_bytes. Pure host
  * computation.
  */
 int ulysses_workspace_size(ulysses_t h, size_t* bytes);
+
+/*
+ * ulysses_set_ds_budget — let the backward keep dS in the workspace when it
+ * fits in `bytes` (default 0: never).
+ *
+ * dQ_i = s * sum_j dS_ij k_j needs the same dS_ij = P_ij (dO_i . v_j - D_i)
+ * that the dK/dV pass forms (HF blog "Ulysses Sequence Parallelism", the
+ * per-head backward of algorithm step 4; the attention backward it runs is
+ * the flash-attention one). With stored dS on, the dK/dV kernel also writes
+ * the bf16 dS of every 128 x 128 block of visible (query, key) pairs, and dQ
+ * becomes one GEMM per block that reads it back, instead of recomputing S
+ * and dP (two more GEMMs and the exponentials). It costs 2 bytes per visible
+ * pair and head: for a causal sequence of sl tokens, about
+ * bs * hc * sl^2 bytes (34.6 GB for sl = 32768, bs = 1, hc = 32).
+ *
+ *   bytes  the budget. Stored dS is on when the dS area of the handle's
+ *          capacity (one causal or full document of cap_sl tokens) is at
+ *          most `bytes` and the tensor-core path applies (bf16, hs = 128);
+ *          off otherwise, and for ulysses_attn_bwd_noalloc always.
+ * Changes ulysses_workspace_size: query it again after this call and pass a
+ * workspace of that size to every later ulysses_attn_bwd / ulysses_layer_bwd.
+ * dK and dV are unchanged bit for bit; dQ agrees with the recomputing path
+ * within bf16 rounding (its dS is formed by the other kernel). Pure host
+ * computation. ULYSSES_ERR_INVALID_ARG for a NULL handle.
+ */
+int ulysses_set_ds_budget(ulysses_t h, size_t bytes);
+
+/*
+ * ulysses_ds_bytes — the stored-dS area of the workspace at capacity: a
+ * 32 KB zero block, then per (rank, batch, query head) 64 KB per visible
+ * pair of (256-key tile, 128-query tile). 0 when stored dS is off. Pure host
+ * computation.
+ */
+int ulysses_ds_bytes(ulysses_t h, size_t* bytes);
 
 /*
  * ulysses_seq_to_head — the first all-to-all: re-shard from sequence to heads.
@@ -467,10 +503,12 @@ int ulysses_timing_read(ulysses_t h, int kernel, double* total_ms, int64_t* laun
  *
  * Limits and sharing:
  *  - A layer whose backward needs more than ULYSSES_NOALLOC_SCRATCH_BYTES of
- *    workspace (see ulysses_workspace_size) is rejected with
- *    ULYSSES_ERR_TOO_LARGE before anything is enqueued. The workspace is 8
- *    bytes per (token, query head, batch element) on the tensor-core path:
- *    64 MiB covers, for example, 256K tokens of a 32-query-head layer.
+ *    workspace (ulysses_workspace_size without the stored-dS area) is
+ *    rejected with ULYSSES_ERR_TOO_LARGE before anything is enqueued. The
+ *    workspace is 8 bytes per (token, query head, batch element) on the
+ *    tensor-core path: 64 MiB covers, for example, 256K tokens of a
+ *    32-query-head layer. This call never stores dS (ulysses_set_ds_budget):
+ *    dQ is recomputed.
  *  - Every call shares the one array, and it keeps the last call's contents.
  *    Each call clears the parts that must start at zero itself. Two calls that
  *    overlap on the GPU (on different streams, or different host threads

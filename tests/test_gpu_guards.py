@@ -85,11 +85,14 @@ def test_no_write_outside_the_buffers(u, sl, bs, hc, hkv, P, causal, offs, fused
             assert not bool(torch.isnan(g.t).any()), f"{k}[{r}]: an output element was never written"
 
 
-def test_lse_and_workspace_stay_in_bounds(u):
-    """The explicit calls with guarded LSE, head shards and workspace."""
+@pytest.mark.parametrize("stored_ds", [False, True])
+def test_lse_and_workspace_stay_in_bounds(u, stored_ds):
+    """The explicit calls with guarded LSE, head shards and workspace (with and without stored dS)."""
     sl, bs, hc, hkv, P = 1000, 1, 4, 2, 2
     dt = torch.bfloat16
     h = u.ulysses_create(sl, bs, hc, hkv, 128, P, True, [0, 333, 1000], dt)
+    u.ulysses_set_ds_budget(h, 1 << 40 if stored_ds else 0)
+    assert (u.ulysses_ds_bytes(h) > 0) == stored_ds
     x = random_inputs(sl, bs, hc, hkv, 128, dt, 77)
     Hq, Hk = hc // P, hkv // P
     heads = {k: [Guarded((sl, bs, H, 128), dt) for _ in range(P)]

@@ -11,10 +11,10 @@ from ._binding import (  # noqa: F401
     ULYSSES_MAX_P, ULYSSES_OK, ULYSSES_NOALLOC_SCRATCH_BYTES, UlyssesError, UlyssesHandle, ulysses_attn_bwd,
     ulysses_attn_bwd_noalloc, ulysses_attn_fwd,
     ulysses_create, ulysses_destroy, ulysses_get_status, ulysses_head_to_seq, ulysses_launch_count, ulysses_seq_to_head,
-    ulysses_strerror, ulysses_workspace_size, ulysses_set_wait_limit, ulysses_inject_fault,
+    ulysses_strerror, ulysses_workspace_size, ulysses_set_ds_budget, ulysses_ds_bytes, ulysses_set_wait_limit, ulysses_inject_fault,
     ulysses_timing_enable, ulysses_timing_read, ULYSSES_KERNEL_COUNT, KERNEL_NAMES,
     ulysses_fused_supported, ulysses_layer_fwd, ulysses_layer_bwd,
     ulysses_host_begin, ulysses_host_step, ulysses_host_end, ulysses_create_varlen, ulysses_set_seq,
     ulysses_seq_to_head_qkv, ulysses_head_to_seq_qkv,
 )
-from .layer import HostSteps, UlyssesLayer  # noqa: F401
+from .layer import HostSteps, UlyssesLayer, default_ds_budget  # noqa: F401

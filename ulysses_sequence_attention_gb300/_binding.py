@@ -67,6 +67,10 @@ lib.ulysses_strerror.argtypes = [ctypes.c_int]
 lib.ulysses_strerror.restype = ctypes.c_char_p
 lib.ulysses_workspace_size.argtypes = [_vp, ctypes.POINTER(ctypes.c_size_t)]
 lib.ulysses_workspace_size.restype = ctypes.c_int
+lib.ulysses_set_ds_budget.argtypes = [_vp, ctypes.c_size_t]
+lib.ulysses_set_ds_budget.restype = ctypes.c_int
+lib.ulysses_ds_bytes.argtypes = [_vp, ctypes.POINTER(ctypes.c_size_t)]
+lib.ulysses_ds_bytes.restype = ctypes.c_int
 lib.ulysses_seq_to_head.argtypes = [_vp, ctypes.c_int, _pp, _pp, _vp]
 lib.ulysses_seq_to_head.restype = ctypes.c_int
 lib.ulysses_head_to_seq.argtypes = [_vp, ctypes.c_int, _pp, _pp, _vp]
@@ -203,6 +207,16 @@ def ulysses_destroy(h: UlyssesHandle):
 def ulysses_workspace_size(h: UlyssesHandle) -> int:
     n = ctypes.c_size_t()
     _check(lib.ulysses_workspace_size(h.ptr, ctypes.byref(n)), "ulysses_workspace_size")
+    return int(n.value)
+
+
+def ulysses_set_ds_budget(h: UlyssesHandle, nbytes: int):
+    _check(lib.ulysses_set_ds_budget(h.ptr, int(nbytes)), "ulysses_set_ds_budget")
+
+
+def ulysses_ds_bytes(h: UlyssesHandle) -> int:
+    n = ctypes.c_size_t()
+    _check(lib.ulysses_ds_bytes(h.ptr, ctypes.byref(n)), "ulysses_ds_bytes")
     return int(n.value)
 
 

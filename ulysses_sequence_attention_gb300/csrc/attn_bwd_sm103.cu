@@ -75,6 +75,9 @@ struct PairParams {
   const float* rows[kRanksPerLaunch];  // dq: the row planes of a rank, [2][bs*Hq][pitch]
   const int2* range;                 // per pair tile: first and last tile of the other side
   const int* order;                  // pair tiles, most work first
+  char* ds;                          // dkdv: stored dS blocks of the launch's first rank, or null
+  const int* ds_base;                // dkdv: first block of each key pair tile in a (rank, batch, head)
+  long long ds_nblk;                 // dkdv: blocks per (rank, batch, head)
   const int32_t* doc_offsets;
   unsigned* status;
   long long timeout;
@@ -110,10 +113,16 @@ constexpr uint32_t kOffK = 0, kOffV = kTile;
 // (all 128 query rows x this CTA's 64 head columns, MN-major).
 constexpr uint32_t kOffStage = 2 * kTile;
 constexpr uint32_t kStage = 4 * kHalf;
-constexpr int NR = 4;                                  // LSE/D row ring
+constexpr int NR = 2;                                  // LSE/D row ring
 constexpr uint32_t kOffRow = kOffStage + NQ * kStage;  // NR x (128 LSE + 128 D) floats
-constexpr uint32_t kOffBar = kOffRow + NR * 1024;
+// Stored dS: this CTA's 128 keys x 128 queries of a tile, [query half][key]
+// [64 queries, 128-byte swizzled], the image the dQ kernel loads verbatim.
+constexpr uint32_t kOffDS = kOffRow + NR * 1024;
+constexpr uint32_t kDSBlock = 2 * kHalf;               // 32 KB
+constexpr uint32_t kOffBar = kOffDS + kDSBlock;
 constexpr uint32_t kSmem = kOffBar + 256;
+static_assert(kOffDS % 1024 == 0, "the swizzled dS image starts 1024-byte aligned");
+static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
 enum {
   B_KV = 0,                  // K, V landed (even CTA: + the odd CTA's forward)
   B_QFULL = 1,               // NQ: query-half part (Qn, dOn) landed (even CTA: + 1 forward)
@@ -129,7 +138,9 @@ enum {
   B_DRAIN = B_EPI + 1,
   B_RFULL = B_DRAIN + 1,     // NR: -LSE/D rows landed (TMA, this CTA)
   B_REMPTY = B_RFULL + NR,   // NR: rows read by this CTA's compute warps (8 warps)
-  B_COUNT = B_REMPTY + NR
+  B_DSFULL = B_REMPTY + NR,  // dS of a tile staged (8 warps)
+  B_DSFREE = B_DSFULL + 1,   // the staged dS has been read by its bulk store (store thread)
+  B_COUNT = B_DSFREE + 1
 };
 static_assert(8 * B_COUNT + 16 + 12 <= 256, "barriers, TMEM slot and key location fit the barrier area");
 }  // namespace dkdv
@@ -173,7 +184,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t cnt = 1;
       if (i == B_KV || (i >= B_HFULL && i < B_HFULL + NQ) || (i >= B_QFULL && i < B_QFULL + NQ))
         cnt = crank == 0 ? 2 : 1;
-      if (i == B_EPI || (i >= B_REMPTY && i < B_REMPTY + NR)) cnt = 8;
+      if (i == B_EPI || i == B_DSFULL || (i >= B_REMPTY && i < B_REMPTY + NR)) cnt = 8;
       if (i == B_P || i == B_SFREE) cnt = 16;
       mbar_init(bar(i), cnt);
     }
@@ -223,17 +234,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int hq = hk * p.group + it / nm;
           const int q0 = (qr.x + it % nm) * 128;
           const uint32_t sq = sb + kOffStage + st * kStage;
-          // -LSE (log2 units) and D of the tile's 128 query rows, one TMA box
-          // from the two row planes. Rows past sl read as zero; every key masks
-          // them, so P = 0 there and dS = 0.
-          const int rsl = it % NR;
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_REMPTY + rsl), ((it / NR) & 1) ^ 1, lim));
-          if (!ok) break;
-          if (lane == 0) {
-            mbar_expect_tx(bar(B_RFULL + rsl), 1024);
-            tma_load_3d(sb + kOffRow + rsl * 1024, &p.tr[rl], bar(B_RFULL + rsl), q0, b * p.Hq + hq, 0);
-          }
-          n_r = it + 1;
           // query-half part: Q and dO rows [q0 + 64c, +64) (B of S^T, dP^T: N = queries)
           ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QEMPTY + st), (u & 1) ^ 1, lim));
           if (!ok) break;
@@ -247,6 +247,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             tma_load_4d(sq + kHalf + kHalf / 2, &p.td[l.map], bar(B_QFULL + st), 64, l.head, b, qh);
           }
           n_q = it + 1;
+          // -LSE (log2 units) and D of the tile's 128 query rows, one TMA box
+          // from the two row planes, needed only once S^T of the tile is
+          // done. Rows past sl read as zero; every key masks them, so P = 0
+          // there and dS = 0.
+          const int rsl = it % NR;
+          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_REMPTY + rsl), ((it / NR) & 1) ^ 1, lim));
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_expect_tx(bar(B_RFULL + rsl), 1024);
+            tma_load_3d(sb + kOffRow + rsl * 1024, &p.tr[rl], bar(B_RFULL + rsl), q0, b * p.Hq + hq, 0);
+          }
+          n_r = it + 1;
         }
         if (it >= 1) {
           // head-half part of tile it-1: Q and dO columns [64c, 64c+64) of all 128 rows (B of dK, dV)
@@ -384,6 +396,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) pair_status(p);
       }
       __syncwarp();
+    } else if (warp == 11 && p.ds) {
+      // --------------------------------------------------------- dS store (both CTAs)
+      // Block (key pair np, query tile m) of a (rank, batch, head) is 64 KB:
+      // the even CTA's 32 KB image, then the odd CTA's.
+      if (lane == 0) {
+        const uint64_t pol = l2_evict_first();
+        const long long first = p.ds_base[np];
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+          if (!mbar_wait(bar(B_DSFULL), it & 1, lim)) {
+            ok = false;
+            break;
+          }
+          const int hq = hk * p.group + it / nm;
+          const long long blk = ((long long)(rl * p.bs + b) * p.Hq + hq) * p.ds_nblk + first + it % nm;
+          bulk_store(p.ds + (size_t)(2 * blk + crank) * kDSBlock, sb + kOffDS, kDSBlock, pol);
+          bulk_commit();
+          bulk_wait_read_all();
+          mbar_arrive(bar(B_DSFREE));
+        }
+        if (!ok) pair_status(p);
+      }
+      __syncwarp();
     }
   } else {
     regs_inc<kRegsCompute>();
@@ -466,6 +501,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       warp_arrive_leader(bar(B_P), crank);
+      if (p.ds) {
+        // dS^T row jr = column jr of dS, staged for the store thread once it
+        // has read the previous tile's image out.
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DSFREE), (it & 1) ^ 1, lim));
+        if (!ok) break;
+        stage_row64(sb + kOffDS + h * kHalf, jr, dk);
+        fence_proxy_async_smem();
+        warp_arrive_local(bar(B_DSFULL));
+      }
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DONE), 0, lim));
     if (ok) {
@@ -814,6 +858,214 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
 }
 
+// ===========================================================================
+// dQ from stored dS: pair = 256 queries
+// ===========================================================================
+// When the dK/dV kernel has written dS to the workspace, dQ = s dS K is one
+// GEMM per (query tile, key tile): the CTA pair streams the dS images of its
+// two query tiles (the A operand, MN-major: queries contiguous) and the key
+// tiles' head-dimension halves (B, MN-major) through a ring of stages, with
+// M = 256 UMMAs into one tensor-memory accumulator. No exponentials, no
+// masks: a block the dK/dV kernel did not visit holds no visible pair, and
+// reads 32 KB of zeros instead.
+namespace dqs {
+constexpr int kThreads = 192;
+constexpr int NS = 4;
+constexpr uint32_t kDS = 2 * kHalf;            // dS image: [query half][128 keys][64 queries], 32 KB
+constexpr uint32_t kStage = kDS + kHalf;       // + K: [128 keys][this CTA's 64 head columns], 16 KB
+constexpr uint32_t kOffBar = NS * kStage;
+constexpr uint32_t kSmem = kOffBar + 256;
+static_assert(kStage % 1024 == 0 && kSmem <= 227 * 1024, "stages 1024-byte aligned, within shared memory");
+enum {
+  B_FULL = 0,                // NS: dS image and K landed (even CTA: + forward)
+  B_EMPTY = B_FULL + NS,     // NS: stage read by its UMMAs (commit, both)
+  B_DONE = B_EMPTY + NS,     // every UMMA done (commit, both)
+  B_EPI = B_DONE + 1,        // dQ staged (4 warps)
+  B_DRAIN = B_EPI + 1,
+  B_COUNT
+};
+}  // namespace dqs
+
+struct DqsParams {
+  CUtensorMap tk[kRanksPerLaunch];   // K, boxes of 64 head columns x 128 rows
+  CUtensorMap tq[kRanksPerLaunch];   // dQ (store), boxes of 64 x 128
+  const int2* range;                 // per query pair tile: first and last key tile
+  const int* order;                  // query pair tiles, most work first
+  const int2* kv_range;              // per key pair tile: the query tiles holding stored blocks
+  const int* ds_base;                // per key pair tile: its first block in a (rank, batch, head)
+  const char* ds;                    // blocks of the launch's first rank
+  const char* zero;                  // 32 KB of zeros
+  long long ds_nblk;                 // blocks per (rank, batch, head)
+  unsigned* status;
+  long long timeout;
+  int bs, Hq, Hk, group, nranks, fused, n;
+  float scale;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(dqs::kThreads, 1)
+    attn_bwd_dq_stored_kernel(const __grid_constant__ DqsParams p) {
+  using namespace dqs;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sb = smem_u32(smem);
+  if (sb & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.status, STATUS_TIMEOUT);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * B_COUNT);
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  auto fail = [&]() { atomicOr(p.status, STATUS_TIMEOUT); };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_rank();
+
+  // Pair work item: (query pair tile, rank, batch, query head).
+  const int pair = blockIdx.x >> 1;
+  const int units = p.nranks * p.bs * p.Hq;
+  const int mp = p.order[pair / units];
+  int rest = pair % units;
+  const int hq = rest % p.Hq;
+  rest /= p.Hq;
+  const int b = rest % p.bs;
+  const int rl = rest / p.bs;
+  const int hk = hq / p.group;
+  const int2 kr = p.range[mp];
+  const int n_kv = kr.y - kr.x + 1;
+  const int m = 2 * mp + (int)crank;  // this CTA's query tile
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < B_COUNT; ++i) {
+      uint32_t cnt = 1;
+      if (i >= B_FULL && i < B_FULL + NS) cnt = crank == 0 ? 2 : 1;
+      if (i == B_EPI) cnt = 4;
+      mbar_init(bar(i), cnt);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc2(smem_u32(tmem_slot), 128);
+    tmem_relinquish2();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const long long lim = p.timeout;
+
+  if (warp == 4) {
+    // ----------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first();
+      const long long unit = (long long)(rl * p.bs + b) * p.Hq + hq;
+      bool ok = true;
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % NS, u = j / NS;
+        if (!mbar_wait(bar(B_EMPTY + st), (u & 1) ^ 1, lim)) {
+          ok = false;
+          break;
+        }
+        const int kt = kr.x + j, np = kt >> 1;
+        const int2 qr = p.kv_range[np];
+        const char* src = p.zero;
+        if (m >= qr.x && m <= qr.y)
+          src = p.ds + (size_t)(2 * (unit * p.ds_nblk + p.ds_base[np] + (m - qr.x)) + (kt & 1)) * kDS;
+        const uint32_t sst = sb + st * kStage;
+        mbar_expect_tx(bar(B_FULL + st), kStage);
+        bulk_load(sst, src, kDS, bar(B_FULL + st), pol);
+        const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hk, hk, kt * 128);
+        tma_load_4d(sst + kDS, &p.tk[l.map], bar(B_FULL + st), 64 * (int)crank, l.head, b, l.row);
+      }
+      if (!ok) fail();
+      for (int i = 0; i < NS; ++i)  // no copy in flight at exit
+        if (n_kv > i) mbar_wait(bar(B_FULL + i), ((n_kv - 1 - i) / NS) & 1, lim);
+    }
+    __syncwarp();
+  } else if (warp == 5 && crank == 0) {
+    // ----------------------------------------------------------- UMMA issuer (even CTA)
+    if (lane == 0) {
+      constexpr uint32_t id = idesc_bf16_f32(256, 128, 1, 1);
+      bool ok = true;
+      for (int j = 0; j < n_kv; ++j) {
+        const int st = j % NS, u = j / NS;
+        if (!mbar_wait(bar(B_FULL + st), u & 1, lim)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sst = sb + st * kStage;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // keys [16kk, 16kk+16): 16 rows of 128 bytes in both operands
+          umma2_ss(tmem, sdesc_sw128(sst + kk * 2048, kHalf, 1024), sdesc_sw128(sst + kDS + kk * 2048, kHalf, 1024),
+                   id, (j > 0 || kk > 0) ? 1u : 0u);
+        umma2_commit_both(bar(B_EMPTY + st));
+      }
+      if (ok)
+        umma2_commit_both(bar(B_DONE));
+      else
+        fail();
+      umma2_commit_both(bar(B_DRAIN));
+      mbar_wait(bar(B_DRAIN), 0, lim);
+    }
+    __syncwarp();
+  } else if (warp == 5 && crank == 1) {
+    // ----------------------------------------------------------- forwarder (odd CTA)
+    if (lane == 0) {
+      bool ok = true;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int st = j % NS, u = j / NS;
+        ok = mbar_wait(bar(B_FULL + st), u & 1, lim);
+        if (ok) mbar_arrive_cluster(mapa(bar(B_FULL + st), 0));
+      }
+      if (!ok) fail();
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ----------------------------------------------------------- epilogue
+    // dQ (times s) of query row iq, staged in stage 0 (free once every UMMA
+    // is done) as two 64-column halves and TMA-stored.
+    const int iq = warp * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DONE), 0, lim));
+    if (ok) {
+      tc_fence_after();
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t o[64], w[32];
+        tmem_ld32(tmem + lane_base + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+        tmem_ld32(tmem + lane_base + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * p.scale, __uint_as_float(o[2 * c + 1]) * p.scale);
+        stage_row64(sb + hh * kHalf, iq, w);
+      }
+      fence_proxy_async_smem();
+      warp_arrive_local(bar(B_EPI));
+      if (threadIdx.x == 0) {
+        if (mbar_wait(bar(B_EPI), 0, lim)) {
+          const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hq, hq, m * 128);
+          tma_store_4d(&p.tq[l.map], sb, 0, l.head, b, l.row);
+          tma_store_4d(&p.tq[l.map], sb + kHalf, 64, l.head, b, l.row);
+          bulk_commit();
+          bulk_wait_read_all();
+        } else {
+          fail();
+        }
+      }
+    } else if (lane == 0) {
+      fail();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc2(tmem, 128);
+  }
+}
+
 // The row planes of the backward, for every (rank, batch, head, row):
 // -LSE * log2(e) (plane 0) and D = rowsum(dO * O) (plane 1), each
 // [bs][Hq][pitch] fp32. 16 lanes per row. O and dO are head shards, or
@@ -824,6 +1076,7 @@ struct PrepParams {
   const __nv_bfloat16* dO[ULYSSES_MAX_P];
   const float* lse[ULYSSES_MAX_P];
   float* rows[ULYSSES_MAX_P];
+  uint4* zero;                       // 32 KB to clear (the stored-dS zero block), or null
   int P, sl, bs, Hq, pitch;
   int fused, n;
 };
@@ -839,6 +1092,10 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constan
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int half = lane >> 4, part = lane & 15;
   const int t0 = blockIdx.x * kPrepRows + warp * 8;
+  if (a.zero && blockIdx.x == 0 && blockIdx.y == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a.zero[i * 256 + threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
+  }
   const long long triples = (long long)a.P * a.bs * a.Hq;
   for (long long y = blockIdx.y; y < triples; y += gridDim.y) {
     const int hq = (int)(y % a.Hq), b = (int)((y / a.Hq) % a.bs), r = (int)(y / ((long long)a.Hq * a.bs));
@@ -929,13 +1186,71 @@ void plan_pair_tiles(const Layer& L, std::vector<int2>& kv_pairs, std::vector<in
   order_by(q_pairs, q_order);
 }
 
+int64_t plan_ds_blocks(const std::vector<int2>& kv_pairs, std::vector<int>& base) {
+  base.resize(kv_pairs.size());
+  int64_t n = 0;
+  for (size_t t = 0; t < kv_pairs.size(); ++t) {
+    base[t] = (int)n;
+    n += kv_pairs[t].y - kv_pairs[t].x + 1;
+  }
+  return n;
+}
+
 int64_t bwd_row_pitch(const Layer& L) { return (L.sl + 3) / 4 * 4; }
 size_t bwd_sm103_workspace(const Layer& L) { return (size_t)L.P * 2 * L.bs * L.Hq * bwd_row_pitch(L) * sizeof(float); }
+// The stored-dS area starts after the row planes of the capacity, so its
+// place does not move with the sequence: first a 32 KB zero block, then per
+// (rank, batch, head) nblk blocks of 64 KB.
+size_t bwd_ds_offset(const Layer& L) {
+  const size_t rows = (size_t)L.P * 2 * L.bs * L.Hq * ((L.cap_sl + 3) / 4 * 4) * sizeof(float);
+  return (rows + 1023) / 1024 * 1024;
+}
+size_t bwd_ds_bytes(const Layer& L, int64_t nblk) {
+  return (size_t)dkdv::kDSBlock + (size_t)L.bs * L.hc * (size_t)nblk * 2 * dkdv::kDSBlock;
+}
 
+
+// dQ of ranks [r0, r0 + nr) from the stored dS blocks (R rows per tensor
+// map, mk kv heads and mq query heads per map, as for the other passes).
+static int launch_dq_stored(const Layer& L, const void* const* k, void* const* dq, const char* ds, const char* zero,
+                            int r0, int nr, int64_t R, int mk, int mq, bool fused, cudaStream_t stream) {
+  DqsParams d;
+  for (int i = 0; i < nr; ++i) {
+    const int r = r0 + i;
+    if (!make_tmap_bf16_4d(&d.tk[i], k[r], 128, mk, L.bs, R, 64, 128) ||
+        !make_tmap_bf16_4d(&d.tq[i], dq[r], 128, mq, L.bs, R, 64, 128))
+      return ULYSSES_ERR_CUDA;
+  }
+  d.range = L.d_qp_range;
+  d.order = L.d_qp_order;
+  d.kv_range = L.d_kvp_range;
+  d.ds_base = L.d_ds_base;
+  d.ds = ds;
+  d.zero = zero;
+  d.ds_nblk = L.ds_nblk;
+  d.status = L.d_status;
+  d.timeout = L.timeout_cycles;
+  d.bs = (int)L.bs;
+  d.Hq = L.Hq;
+  d.Hk = L.Hk;
+  d.group = L.Hq / L.Hk;
+  d.nranks = nr;
+  d.fused = fused ? 1 : 0;
+  d.n = (int)L.n();
+  d.scale = (float)(1.0 / sqrt((double)L.hs));
+  const long long pairs = (long long)((L.sl + 255) / 256) * nr * L.bs * L.Hq;
+  if (2 * pairs > 0x7fffffffLL) return ULYSSES_ERR_UNSUPPORTED;
+  Timed t(L.timing, ULYSSES_KERNEL_BWD_DQ, stream);
+  attn_bwd_dq_stored_kernel<<<(unsigned)(2 * pairs), dqs::kThreads, dqs::kSmem, stream>>>(d);
+  t.done();
+  count_launches(1);
+  return ULYSSES_OK;
+}
 
 int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* const* k, const void* const* v,
                           const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,
-                          void* const* dk, void* const* dv, void* workspace, cudaStream_t stream, bool fused) {
+                          void* const* dk, void* const* dv, void* workspace, cudaStream_t stream, bool fused,
+                          bool store_ds) {
   if (fused && !fused_supported(L)) return ULYSSES_ERR_UNSUPPORTED;
   static PerDeviceOnce attrs;
   const int ast = attrs.run([] {
@@ -943,6 +1258,9 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
         cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dkdv::kSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dqk::kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_bwd_dq_stored_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)dqs::kSmem);
     return e;
   });
   if (ast != ULYSSES_OK) return ast;
@@ -952,6 +1270,11 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
   const long long pitch = bwd_row_pitch(L);
   const long long nrows = (long long)L.bs * L.Hq;
   const long long per_rank = 2 * nrows * pitch;
+  // Stored dS: the zero block, then the blocks of every (rank, batch, head).
+  store_ds = store_ds && L.ds_on;
+  char* ds_zero = store_ds ? reinterpret_cast<char*>(workspace) + bwd_ds_offset(L) : nullptr;
+  char* ds = store_ds ? ds_zero + dkdv::kDSBlock : nullptr;
+  const size_t ds_per_rank = (size_t)L.bs * L.Hq * (size_t)L.ds_nblk * 2 * dkdv::kDSBlock;
 
   // 1. The row planes.
   {
@@ -969,6 +1292,7 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
     a.pitch = (int)pitch;
     a.fused = fused ? 1 : 0;
     a.n = (int)L.n();
+    a.zero = reinterpret_cast<uint4*>(ds_zero);
     Timed t(L.timing, ULYSSES_KERNEL_BWD_PREP, stream);
     const long long triples = (long long)L.P * L.bs * L.Hq;
     const dim3 grid((unsigned)((L.sl + kPrepRows - 1) / kPrepRows), (unsigned)std::min(triples, 65535LL));
@@ -991,6 +1315,8 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
   prm.fused = fused ? 1 : 0;
   prm.n = (int)L.n();
   prm.skip_q_loads = 0;
+  prm.ds_base = L.d_ds_base;
+  prm.ds_nblk = L.ds_nblk;
   const bool inject = L.inject_fault == 2;
   if (inject) L.inject_fault = 0;
   prm.scale = (float)(1.0 / sqrt((double)L.hs));
@@ -1005,7 +1331,13 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
     prm.order = pass == 0 ? L.d_kvp_order : L.d_qp_order;
     for (int r0 = 0; r0 < L.P; r0 += kRanksPerLaunch) {
       const int nr = std::min(kRanksPerLaunch, L.P - r0);
+      if (pass == 1 && store_ds) {
+        const int st = launch_dq_stored(L, k, dq, ds + ds_per_rank * r0, ds_zero, r0, nr, R, mk, mq, fused, stream);
+        if (st != ULYSSES_OK) return st;
+        continue;
+      }
       prm.nranks = nr;
+      prm.ds = (pass == 0 && store_ds) ? ds + ds_per_rank * r0 : nullptr;
       prm.skip_q_loads = (inject && pass == 0) ? 1 : 0;
       for (int i = 0; i < nr; ++i) {
         const int r = r0 + i;

@@ -111,6 +111,9 @@ static cudaError_t upload_seq(Layer& L, cudaStream_t stream, bool async) {
     std::vector<int2> kvp, qp;
     std::vector<int> kvo, qo;
     uly::plan_pair_tiles(L, kvp, kvo, qp, qo);
+    std::vector<int> ds_base;
+    L.ds_nblk = uly::plan_ds_blocks(kvp, ds_base);
+    if (e == cudaSuccess) e = copy(L.d_ds_base, ds_base.data(), sizeof(int) * ds_base.size());
     if (e == cudaSuccess) e = copy(L.d_kvp_range, kvp.data(), sizeof(int2) * kvp.size());
     if (e == cudaSuccess) e = copy(L.d_kvp_order, kvo.data(), sizeof(int) * kvo.size());
     if (e == cudaSuccess) e = copy(L.d_qp_range, qp.data(), sizeof(int2) * qp.size());
@@ -127,6 +130,7 @@ static void free_layer(Layer* L) {
   cudaFree(L->d_kvp_order);
   cudaFree(L->d_qp_range);
   cudaFree(L->d_qp_order);
+  cudaFree(L->d_ds_base);
   delete L;
 }
 
@@ -161,6 +165,7 @@ static int create_layer(ulysses_t* out, int64_t sl, int64_t bs, int hc, int hkv,
     if (e == cudaSuccess) e = cudaMalloc(&L->d_kvp_order, sizeof(int) * n_pair);
     if (e == cudaSuccess) e = cudaMalloc(&L->d_qp_range, sizeof(int2) * n_pair);
     if (e == cudaSuccess) e = cudaMalloc(&L->d_qp_order, sizeof(int) * n_pair);
+    if (e == cudaSuccess) e = cudaMalloc(&L->d_ds_base, sizeof(int) * n_pair);
   }
   if (e == cudaSuccess) e = upload_seq(*L, 0, false);
   if (e != cudaSuccess) {
@@ -234,20 +239,23 @@ void ulysses_destroy(ulysses_t h) {
 int ulysses_workspace_size(ulysses_t h, size_t* bytes) {
   const Layer* L = reinterpret_cast<const Layer*>(h);
   if (!L || !bytes) return ULYSSES_ERR_INVALID_ARG;
-  // Tensor-core path: per rank two fp32 row planes, -LSE*log2(e) and
-  // D = rowsum(dO * O), [bs][Hq][sl rounded up to 4] each. Other paths: D only,
-  // [P][bs][Hq][sl].
-  // Sized for the handle's capacity (its own sl unless made by
-  // ulysses_create_varlen), so one workspace serves every ulysses_set_seq.
-  Layer cap;
-  cap.sl = L->cap_sl;
-  cap.bs = L->bs;
-  cap.P = L->P;
-  cap.Hq = L->Hq;
-  cap.hs = L->hs;
-  cap.dtype = L->dtype;
-  *bytes = uly::fwd_sm103_supported(cap) ? uly::bwd_sm103_workspace(cap)
-                                         : (size_t)cap.P * cap.bs * cap.Hq * cap.sl * sizeof(float);
+  *bytes = uly::workspace_bytes(*L, L->ds_on);
+  return ULYSSES_OK;
+}
+
+int ulysses_set_ds_budget(ulysses_t h, size_t bytes) {
+  Layer* L = reinterpret_cast<Layer*>(h);
+  if (!L) return ULYSSES_ERR_INVALID_ARG;
+  L->ds_budget = bytes;
+  const int64_t nblk = uly::ds_blocks_at_capacity(*L);
+  L->ds_on = nblk > 0 && uly::bwd_ds_bytes(*L, nblk) <= bytes;
+  return ULYSSES_OK;
+}
+
+int ulysses_ds_bytes(ulysses_t h, size_t* bytes) {
+  const Layer* L = reinterpret_cast<const Layer*>(h);
+  if (!L || !bytes) return ULYSSES_ERR_INVALID_ARG;
+  *bytes = L->ds_on ? uly::bwd_ds_bytes(*L, uly::ds_blocks_at_capacity(*L)) : 0;
   return ULYSSES_OK;
 }
 
@@ -328,6 +336,50 @@ int ulysses_attn_bwd(ulysses_t h, const void* const* q, const void* const* k,
                      const void* const* v, const void* const* o, const void* const* dO,
                      const float* const* lse, void* const* dq, void* const* dk, void* const* dv,
                      void* workspace, void* stream) {
+  return uly::attn_bwd_entry(h, q, k, v, o, dO, lse, dq, dk, dv, workspace, stream, true);
+}
+
+}  // extern "C"
+
+namespace uly {
+
+size_t workspace_bytes(const Layer& L, bool with_ds) {
+  // Tensor-core path: per rank two fp32 row planes, -LSE*log2(e) and
+  // D = rowsum(dO * O), [bs][Hq][sl rounded up to 4] each, then (stored dS)
+  // the zero block and the dS blocks. Other paths: D only, [P][bs][Hq][sl].
+  // Sized for the handle's capacity (its own sl unless made by
+  // ulysses_create_varlen), so one workspace serves every ulysses_set_seq.
+  Layer cap;
+  cap.sl = L.cap_sl;
+  cap.bs = L.bs;
+  cap.P = L.P;
+  cap.Hq = L.Hq;
+  cap.hs = L.hs;
+  cap.dtype = L.dtype;
+  if (!fwd_sm103_supported(cap)) return (size_t)cap.P * cap.bs * cap.Hq * cap.sl * sizeof(float);
+  if (!with_ds) return bwd_sm103_workspace(cap);
+  return bwd_ds_offset(L) + bwd_ds_bytes(L, ds_blocks_at_capacity(L));
+}
+
+// Stored-dS blocks per (rank, batch, head) of the longest sequence the handle
+// takes: one document of cap_sl tokens (documents only narrow the ranges).
+// 0 when the tensor-core path does not apply or the count leaves int range.
+int64_t ds_blocks_at_capacity(const Layer& L) {
+  if (!fwd_sm103_supported(L) || L.cap_sl <= 0 || L.bs <= 0) return 0;
+  Layer cap;
+  cap.sl = L.cap_sl;
+  cap.causal = L.causal;
+  cap.doc_offsets = {0, (int32_t)L.cap_sl};
+  std::vector<int2> kvp, qp;
+  std::vector<int> kvo, qo, base;
+  plan_pair_tiles(cap, kvp, kvo, qp, qo);
+  const int64_t n = plan_ds_blocks(kvp, base);
+  return n < 0x7fffffffLL ? n : 0;
+}
+
+int attn_bwd_entry(ulysses_t h, const void* const* q, const void* const* k, const void* const* v,
+                   const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,
+                   void* const* dk, void* const* dv, void* workspace, void* stream, bool store_ds) {
   const Layer* L = reinterpret_cast<const Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
   if (L->empty()) return ULYSSES_OK;
@@ -342,11 +394,15 @@ int ulysses_attn_bwd(ulysses_t h, const void* const* q, const void* const* k,
   CHECK_PTRS(dv);
   if (!workspace) return ULYSSES_ERR_INVALID_ARG;
   if (((uintptr_t)workspace) & 15u) return ULYSSES_ERR_ALIGNMENT;
-  if (uly::fwd_sm103_supported(*L))
-    return uly::launch_attn_bwd_sm103(*L, q, k, v, o, dO, lse, dq, dk, dv, workspace, (cudaStream_t)stream);
-  return uly::launch_attn_bwd_simt(*L, q, k, v, o, dO, lse, dq, dk, dv, workspace,
-                                   (cudaStream_t)stream);
+  if (fwd_sm103_supported(*L))
+    return launch_attn_bwd_sm103(*L, q, k, v, o, dO, lse, dq, dk, dv, workspace, (cudaStream_t)stream, false,
+                                 store_ds);
+  return launch_attn_bwd_simt(*L, q, k, v, o, dO, lse, dq, dk, dv, workspace, (cudaStream_t)stream);
 }
+
+}  // namespace uly
+
+extern "C" {
 
 int ulysses_fused_supported(ulysses_t h) {
   const Layer* L = reinterpret_cast<const Layer*>(h);
@@ -386,7 +442,8 @@ int ulysses_layer_bwd(ulysses_t h, const void* const* q, const void* const* k, c
   CHECK_PTRS(dv);
   if (!workspace) return ULYSSES_ERR_INVALID_ARG;
   if (((uintptr_t)workspace) & 15u) return ULYSSES_ERR_ALIGNMENT;
-  return uly::launch_attn_bwd_sm103(*L, q, k, v, o, dO, lse, dq, dk, dv, workspace, (cudaStream_t)stream, true);
+  return uly::launch_attn_bwd_sm103(*L, q, k, v, o, dO, lse, dq, dk, dv, workspace, (cudaStream_t)stream, true,
+                                    true);
 }
 
 int ulysses_set_wait_limit(ulysses_t h, int64_t cycles) {

@@ -134,6 +134,16 @@ struct Layer {
   int* d_kvp_order = nullptr;
   int2* d_qp_range = nullptr;
   int* d_qp_order = nullptr;
+  // Stored dS (ulysses_set_ds_budget): the dK/dV kernel also writes the bf16
+  // dS of every visible (128-key tile, 128-query tile) block to the
+  // workspace, and dQ = s dS K reads it back instead of recomputing S and dP.
+  // Per 256-key pair tile, the index of its first block within a (rank,
+  // batch, head); ds_nblk blocks per (rank, batch, head) for the current
+  // sequence. On when the capacity's dS fits the budget.
+  int* d_ds_base = nullptr;
+  int64_t ds_nblk = 0;
+  size_t ds_budget = 0;
+  bool ds_on = false;
   long long timeout_cycles = 4000000000LL;  // bound of every device-side wait (~2 s)
   mutable int inject_fault = 0;             // test hook (ulysses_inject_fault), consumed by one call
   mutable Timing timing;                    // ulysses_timing_enable / ulysses_timing_read
@@ -209,11 +219,21 @@ int launch_attn_fwd_sm103(Layer& L, const void* const* q, const void* const* k, 
 
 void plan_pair_tiles(const Layer& L, std::vector<int2>& kv_pairs, std::vector<int>& kv_order,
                      std::vector<int2>& q_pairs, std::vector<int>& q_order);
+// Stored dS blocks: base[t] = index of the first block of key pair tile t
+// within a (rank, batch, head); returns the blocks per (rank, batch, head).
+int64_t plan_ds_blocks(const std::vector<int2>& kv_pairs, std::vector<int>& base);
+// The row planes of the tensor-core backward.
 size_t bwd_sm103_workspace(const Layer& L);
+// The stored-dS area that follows them (zero block + blocks) for nblk blocks
+// per (rank, batch, head), and its offset in the workspace.
+size_t bwd_ds_bytes(const Layer& L, int64_t nblk);
+size_t bwd_ds_offset(const Layer& L);
 // fused: q, k, v, o, dO, dq, dk, dv are sequence shards (else head shards).
+// store_ds: the workspace holds the stored-dS area (L.ds_on) and may use it.
 int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* const* k, const void* const* v,
                           const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,
-                          void* const* dk, void* const* dv, void* workspace, cudaStream_t s, bool fused = false);
+                          void* const* dk, void* const* dv, void* workspace, cudaStream_t s, bool fused = false,
+                          bool store_ds = false);
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? ULYSSES_OK : ULYSSES_ERR_CUDA; }
 
@@ -236,6 +256,16 @@ struct PerDeviceOnce {
     return ULYSSES_OK;
   }
 };
+
+// Workspace of the backward for the handle's capacity, with or without the
+// stored-dS area; the blocks per (rank, batch, head) at capacity.
+size_t workspace_bytes(const Layer& L, bool with_ds);
+int64_t ds_blocks_at_capacity(const Layer& L);
+// ulysses_attn_bwd; store_ds = false keeps to the row planes of the workspace
+// (the recomputing dQ), whatever the handle's dS budget.
+int attn_bwd_entry(ulysses_t h, const void* const* q, const void* const* k, const void* const* v,
+                   const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,
+                   void* const* dk, void* const* dv, void* workspace, void* stream, bool store_ds);
 
 // Frees the host-streaming streams and events of a handle (host_step.cu).
 void destroy_host_pipe(Layer& L);

@@ -45,12 +45,12 @@ extern "C" int ulysses_attn_bwd_noalloc(ulysses_t h, const void* const* q, const
                                         const float* const* lse, void* const* dq, void* const* dk,
                                         void* const* dv, void* stream) {
   if (!h) return ULYSSES_ERR_INVALID_ARG;
-  size_t need = 0;
-  int st = ulysses_workspace_size(h, &need);
-  if (st != ULYSSES_OK) return st;
+  // The row planes only: dQ is recomputed here even when the handle's dS
+  // budget would store dS.
+  const size_t need = uly::workspace_bytes(*reinterpret_cast<const uly::Layer*>(h), false);
   if (need > (size_t)ULYSSES_NOALLOC_SCRATCH_BYTES) return ULYSSES_ERR_TOO_LARGE;
   void* scratch = nullptr;
-  st = scratch_address(&scratch);
+  const int st = scratch_address(&scratch);
   if (st != ULYSSES_OK) return st;
-  return ulysses_attn_bwd(h, q, k, v, o, dO, lse, dq, dk, dv, scratch, stream);
+  return uly::attn_bwd_entry(h, q, k, v, o, dO, lse, dq, dk, dv, scratch, stream, false);
 }

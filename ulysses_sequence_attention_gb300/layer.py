@@ -19,6 +19,11 @@ Two ways to run them, both through the C-ABI of libulysses.so:
 Both give bit-identical results. This class only owns the intermediate buffers
 (torch device memory) and enqueues the calls on the current stream.
 
+The backward's workspace also holds dS when the whole dS of the layer's
+capacity fits its dS budget (ulysses_set_ds_budget; by default up to 64 GiB
+and a quarter of the device): the dK/dV kernel writes it and dQ reads it
+back, instead of recomputing S and dP.
+
 HostSteps runs whole training steps from host memory (ulysses_host_*): inputs
 in, forward and backward, outputs out, with the copies overlapped with the
 neighbouring steps' kernels.
@@ -33,12 +38,32 @@ import torch
 from . import _binding as B
 
 
+# Stored dS takes at most this much, and at most a quarter of the device.
+DS_BUDGET_CAP = 64 << 30
+
+
+def default_ds_budget(device="cuda") -> int:
+    """The dS budget a layer gets unless told otherwise."""
+    if not torch.cuda.is_available():
+        return 0
+    total = torch.cuda.get_device_properties(torch.device(device)).total_memory
+    return min(DS_BUDGET_CAP, total // 4)
+
+
 class UlyssesLayer:
     def __init__(self, sl: int, bs: int, hc: int, hkv: int, hs: int, P: int, causal: bool = True,
                  doc_offsets: Optional[Sequence[int]] = None, dtype=torch.bfloat16,
-                 device: str = "cuda", fused: Optional[bool] = None, _handle=None):
-        """fused: None picks the fused path when the shape allows it; True requires it."""
+                 device: str = "cuda", fused: Optional[bool] = None, ds_budget: Optional[int] = None,
+                 _handle=None):
+        """fused: None picks the fused path when the shape allows it; True requires it.
+
+        ds_budget: bytes the backward may keep dS in (ulysses_set_ds_budget);
+        None = default_ds_budget(device). dQ then reads dS back instead of
+        recomputing it, when the whole dS of the capacity fits.
+        """
         self.h = _handle or B.ulysses_create(sl, bs, hc, hkv, hs, P, causal, doc_offsets, dtype)
+        B.ulysses_set_ds_budget(self.h, default_ds_budget(device) if ds_budget is None else int(ds_budget))
+        self.stores_ds = B.ulysses_ds_bytes(self.h) > 0
         self.cap_sl = getattr(self.h, "max_sl", sl)
         self.sl, self.bs, self.hc, self.hkv, self.hs, self.P = sl, bs, hc, hkv, hs, P
         self.dtype = dtype
@@ -52,14 +77,14 @@ class UlyssesLayer:
     @classmethod
     def variable_length(cls, max_sl: int, bs: int, hc: int, hkv: int, hs: int, P: int, causal: bool = True,
                         max_docs: int = 1, dtype=torch.bfloat16, device: str = "cuda",
-                        fused: Optional[bool] = None) -> "UlyssesLayer":
+                        fused: Optional[bool] = None, ds_budget: Optional[int] = None) -> "UlyssesLayer":
         """A layer for batches of varying length (the pages' seq_length_is_variable=True).
 
         Starts empty; call set_seq before each batch of a new length or packing.
         Buffers are sized for max_sl once, so a new length allocates nothing.
         """
         h = B.ulysses_create_varlen(max_sl, bs, hc, hkv, hs, P, causal, max_docs, dtype)
-        return cls(0, bs, hc, hkv, hs, P, causal, None, dtype, device, fused, _handle=h)
+        return cls(0, bs, hc, hkv, hs, P, causal, None, dtype, device, fused, ds_budget, _handle=h)
 
     def set_seq(self, sl: int, doc_offsets: Optional[Sequence[int]] = None, stream=None):
         """Switch to a sequence of sl tokens (packed at doc_offsets), in order on `stream`."""
