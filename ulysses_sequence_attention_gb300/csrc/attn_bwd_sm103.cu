@@ -113,16 +113,20 @@ constexpr uint32_t kOffK = 0, kOffV = kTile;
 // (all 128 query rows x this CTA's 64 head columns, MN-major).
 constexpr uint32_t kOffStage = 2 * kTile;
 constexpr uint32_t kStage = 4 * kHalf;
-constexpr int NR = 2;                                  // LSE/D row ring
-constexpr uint32_t kOffRow = kOffStage + NQ * kStage;  // NR x (128 LSE + 128 D) floats
-// Stored dS: this CTA's 128 keys x 128 queries of a tile, [query half][key]
-// [64 queries, 128-byte swizzled], the image the dQ kernel loads verbatim.
-constexpr uint32_t kOffDS = kOffRow + NR * 1024;
+constexpr uint32_t kOffRow = kOffStage + NQ * kStage;  // LSE/D row ring: NR x (128 LSE + 128 D) floats
 constexpr uint32_t kDSBlock = 2 * kHalf;               // 32 KB
-constexpr uint32_t kOffBar = kOffDS + kDSBlock;
-constexpr uint32_t kSmem = kOffBar + 256;
-static_assert(kOffDS % 1024 == 0, "the swizzled dS image starts 1024-byte aligned");
-static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
+// With stored dS (kStore) the row ring gives up two of its four slots to the
+// dS image: this CTA's 128 keys x 128 queries of a tile, [query half][key]
+// [64 queries, 128-byte swizzled], the image the dQ kernel loads verbatim.
+template <bool kStore>
+struct Layout {
+  static constexpr int NR = kStore ? 2 : 4;
+  static constexpr uint32_t kOffDS = kOffRow + NR * 1024;
+  static constexpr uint32_t kOffBar = kOffDS + (kStore ? kDSBlock : 0u);
+  static constexpr uint32_t kSmem = kOffBar + 256;
+  static_assert(kOffDS % 1024 == 0, "the swizzled dS image starts 1024-byte aligned");
+  static_assert(kSmem <= 227 * 1024, "shared memory of one CTA");
+};
 enum {
   B_KV = 0,                  // K, V landed (even CTA: + the odd CTA's forward)
   B_QFULL = 1,               // NQ: query-half part (Qn, dOn) landed (even CTA: + 1 forward)
@@ -137,17 +141,21 @@ enum {
   B_EPI = B_DONE + 1,        // dK, dV staged (8 warps)
   B_DRAIN = B_EPI + 1,
   B_RFULL = B_DRAIN + 1,     // NR: -LSE/D rows landed (TMA, this CTA)
-  B_REMPTY = B_RFULL + NR,   // NR: rows read by this CTA's compute warps (8 warps)
-  B_DSFULL = B_REMPTY + NR,  // dS of a tile staged (8 warps)
-  B_DSFREE = B_DSFULL + 1,   // the staged dS has been read by its bulk store (store thread)
-  B_COUNT = B_DSFREE + 1
+  // then B_REMPTY (NR): rows read by this CTA's compute warps (8 warps);
+  // with stored dS, B_DSFULL: dS of a tile staged (8 warps), and B_DSFREE:
+  // the staged dS has been read by its bulk store (store thread)
 };
-static_assert(8 * B_COUNT + 16 + 12 <= 256, "barriers, TMEM slot and key location fit the barrier area");
 }  // namespace dkdv
 
+template <bool kStore>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ PairParams p) {
   using namespace dkdv;
+  constexpr int NR = Layout<kStore>::NR;
+  constexpr uint32_t kOffDS = Layout<kStore>::kOffDS, kOffBar = Layout<kStore>::kOffBar;
+  constexpr int B_REMPTY = B_RFULL + NR, B_DSFULL = B_REMPTY + NR, B_DSFREE = B_DSFULL + 1;
+  constexpr int B_COUNT = B_DSFREE + 1;
+  static_assert(8 * B_COUNT + 16 + 12 <= 256, "barriers, TMEM slot and key location fit the barrier area");
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
   if (sb & 1023u) {  // same condition in both CTAs: both leave before any cluster barrier
@@ -396,7 +404,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) pair_status(p);
       }
       __syncwarp();
-    } else if (warp == 11 && p.ds) {
+    } else if (kStore && warp == 11) {
       // --------------------------------------------------------- dS store (both CTAs)
       // Block (key pair np, query tile m) of a (rank, batch, head) is 64 KB:
       // the even CTA's 32 KB image, then the odd CTA's.
@@ -501,7 +509,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       warp_arrive_leader(bar(B_P), crank);
-      if (p.ds) {
+      if (kStore) {
         // dS^T row jr = column jr of dS, staged for the store thread once it
         // has read the previous tile's image out.
         ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DSFREE), (it & 1) ^ 1, lim));
@@ -1254,8 +1262,11 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
   if (fused && !fused_supported(L)) return ULYSSES_ERR_UNSUPPORTED;
   static PerDeviceOnce attrs;
   const int ast = attrs.run([] {
-    cudaError_t e =
-        cudaFuncSetAttribute(attn_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dkdv::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)dkdv::Layout<false>::kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)dkdv::Layout<true>::kSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dqk::kSmem);
     if (e == cudaSuccess)
@@ -1366,8 +1377,10 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
       const long long pairs = (long long)n_pair * nr * L.bs * (pass == 0 ? L.Hk : L.Hq);
       if (2 * pairs > 0x7fffffffLL) return ULYSSES_ERR_UNSUPPORTED;
       Timed t(L.timing, pass == 0 ? ULYSSES_KERNEL_BWD_DKDV : ULYSSES_KERNEL_BWD_DQ, stream);
-      if (pass == 0)
-        attn_bwd_dkdv_kernel<<<(unsigned)(2 * pairs), kThreads, dkdv::kSmem, stream>>>(prm);
+      if (pass == 0 && store_ds)
+        attn_bwd_dkdv_kernel<true><<<(unsigned)(2 * pairs), kThreads, dkdv::Layout<true>::kSmem, stream>>>(prm);
+      else if (pass == 0)
+        attn_bwd_dkdv_kernel<false><<<(unsigned)(2 * pairs), kThreads, dkdv::Layout<false>::kSmem, stream>>>(prm);
       else
         attn_bwd_dq_kernel<<<(unsigned)(2 * pairs), kThreads, dqk::kSmem, stream>>>(prm);
       t.done();
