@@ -363,7 +363,7 @@ def run_ours(args, w, rank, world):
     result = {"ms_per_step": ms_per_step, "value": value, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
               "s2h_qkv_ms": s2h_ms, "h2s_o_ms": h2s_ms, "launches": launches, "clocks": clk, "e2e": e2e,
               "kernels": kernels, "path": "fused" if L.fused else "explicit",
-              "ds_bytes": B.ulysses_ds_bytes(h)}
+              "ds_bytes": B.ulysses_ds_bytes(h)[0] if L.stores_ds else 0}
     return result
 
 

@@ -157,16 +157,16 @@ const char* ulysses_strerror(int status);
  * bf16 with hs = 128 (the tensor-core path): for each rank, two fp32 row
  * planes [bs][hc/P][pitch], -LSE*log2(e) and D = rowsum(dO * O), where pitch
  * is sl rounded up to a multiple of 4: P * 2 * bs * (hc/P) * pitch * 4 bytes.
- * Other configurations: D only, P * bs * (hc/P) * sl * 4 bytes. With stored
- * dS on (ulysses_set_ds_budget), add the stored-dS area after the row planes
- * (at an offset rounded up to 1024 bytes): ulysses_ds_bytes. Pure host
- * computation.
+ * Other configurations: D only, P * bs * (hc/P) * sl * 4 bytes. With a dS
+ * area reserved (ulysses_set_ds_budget), add it after the row planes, at an
+ * offset rounded up to 1024 bytes (`reserved` of ulysses_ds_bytes). Pure
+ * host computation.
  */
 int ulysses_workspace_size(ulysses_t h, size_t* bytes);
 
 /*
- * ulysses_set_ds_budget — let the backward keep dS in the workspace when it
- * fits in `bytes` (default 0: never).
+ * ulysses_set_ds_budget — reserve up to `bytes` of the workspace for keeping
+ * dS (default 0: none).
  *
  * dQ_i = s * sum_j dS_ij k_j needs the same dS_ij = P_ij (dO_i . v_j - D_i)
  * that the dK/dV pass forms (HF blog "Ulysses Sequence Parallelism", the
@@ -176,13 +176,19 @@ int ulysses_workspace_size(ulysses_t h, size_t* bytes);
  * becomes one GEMM per block that reads it back, instead of recomputing S
  * and dP (two more GEMMs and the exponentials). It costs 2 bytes per visible
  * pair and head: for a causal sequence of sl tokens, about
- * bs * hc * sl^2 bytes (34.6 GB for sl = 32768, bs = 1, hc = 32).
+ * bs * hc * sl^2 bytes (34.6 GB for sl = 32768, bs = 1, hc = 32); packed
+ * documents need only their own pairs.
  *
- *   bytes  the budget. Stored dS is on when the dS area of the handle's
- *          capacity (one causal or full document of cap_sl tokens) is at
- *          most `bytes` and the tensor-core path applies (bf16, hs = 128);
- *          off otherwise, and for ulysses_attn_bwd_noalloc always.
- * Changes ulysses_workspace_size: query it again after this call and pass a
+ *   bytes  the budget. The area reserved is a 32 KB zero block plus as many
+ *          64 KB blocks per (rank, batch, query head) as fit in `bytes`, but
+ *          no more than one document of the handle's capacity needs (the
+ *          most any of its sequences can). Nothing is reserved below the
+ *          zero block and one block, or off the tensor-core path (bf16,
+ *          hs = 128).
+ * A backward stores dS when the blocks of the current sequence fit the
+ * reserved area (ulysses_ds_bytes: needed <= reserved), and recomputes dQ
+ * otherwise; ulysses_attn_bwd_noalloc always recomputes. Changes
+ * ulysses_workspace_size: query it again after this call and pass a
  * workspace of that size to every later ulysses_attn_bwd / ulysses_layer_bwd.
  * dK and dV are unchanged bit for bit; dQ agrees with the recomputing path
  * within bf16 rounding (its dS is formed by the other kernel). Pure host
@@ -191,12 +197,16 @@ int ulysses_workspace_size(ulysses_t h, size_t* bytes);
 int ulysses_set_ds_budget(ulysses_t h, size_t bytes);
 
 /*
- * ulysses_ds_bytes — the stored-dS area of the workspace at capacity: a
- * 32 KB zero block, then per (rank, batch, query head) 64 KB per visible
- * pair of (256-key tile, 128-query tile). 0 when stored dS is off. Pure host
- * computation.
+ * ulysses_ds_bytes — stored-dS sizes, in bytes (either pointer may be NULL):
+ *   needed    the area the current sequence uses: a 32 KB zero block, then
+ *             per (rank, batch, query head) 64 KB per visible pair of
+ *             (256-key tile, 128-query tile); 0 off the tensor-core path or
+ *             for an empty sequence.
+ *   reserved  the area reserved in the workspace (ulysses_set_ds_budget), 0
+ *             if none.
+ * Pure host computation. ULYSSES_ERR_INVALID_ARG for a NULL handle.
  */
-int ulysses_ds_bytes(ulysses_t h, size_t* bytes);
+int ulysses_ds_bytes(ulysses_t h, size_t* needed, size_t* reserved);
 
 /*
  * ulysses_seq_to_head — the first all-to-all: re-shard from sequence to heads.

@@ -8,9 +8,9 @@ seeded inputs:
 * both against the fp64 oracle, at the bf16 bar;
 * dK and dV bit for bit the same (the dK/dV kernel's arithmetic does not
   change, it only also stores dS);
-* the workspace grows by exactly the stored-dS area, whose size follows from
-  the block count of the tile schedule: per (rank, batch, head), one 64 KB
-  block per visible (256-key tile, 128-query tile).
+* the workspace grows by exactly the reserved stored-dS area, whose size
+  follows from the block count of the tile schedule: per (rank, batch,
+  head), one 64 KB block per visible (256-key tile, 128-query tile).
 The cases cover a block that one CTA of a pair has and the other lacks (a
 document across the pair), a pair whose odd query tile is past the sequence,
 non-causal documents, replicated kv heads and more ranks than one launch
@@ -80,13 +80,14 @@ def test_stored_ds_against_the_oracle_and_the_recomputing_dq(u, sl, bs, hc, hkv,
     S = u.UlyssesLayer(sl, bs, hc, hkv, 128, P, causal, offs, dt, fused=fused, ds_budget=BIG)
     R = u.UlyssesLayer(sl, bs, hc, hkv, 128, P, causal, offs, dt, fused=fused, ds_budget=0)
     assert S.stores_ds and not R.stores_ds
-    # The capacity is the handle's own sequence; the area is sized for one
-    # document of it (documents only narrow the schedule).
-    want_ds = 32768 + bs * hc * blocks_per_head(sl, causal, None) * 65536
-    assert u.ulysses_ds_bytes(S.h) == want_ds
-    assert u.ulysses_ds_bytes(R.h) == 0
+    # The sequence needs its own blocks; the largest budget reserves what one
+    # document of the capacity (the handle's own length) needs.
+    need = 32768 + bs * hc * blocks_per_head(sl, causal, offs) * 65536
+    cap = 32768 + bs * hc * blocks_per_head(sl, causal, None) * 65536
+    assert u.ulysses_ds_bytes(S.h) == (need, cap)
+    assert u.ulysses_ds_bytes(R.h) == (need, 0)
     rows = u.ulysses_workspace_size(R.h)
-    assert u.ulysses_workspace_size(S.h) == (rows + 1023) // 1024 * 1024 + want_ds
+    assert u.ulysses_workspace_size(S.h) == (rows + 1023) // 1024 * 1024 + cap
 
     got, ref = run(S, x, P), run(R, x, P)
     assert u.ulysses_get_status(S.h) == u.ULYSSES_OK and u.ulysses_get_status(R.h) == u.ULYSSES_OK
@@ -101,19 +102,21 @@ def test_stored_ds_against_the_oracle_and_the_recomputing_dq(u, sl, bs, hc, hkv,
         assert_close(f"{n} recomputed", ref[n], want, dt)
 
 
-def test_budget_threshold_and_noalloc(u):
-    """On exactly when the area fits; the no-alloc entry point recomputes dQ whatever the budget."""
+def test_budget_reserves_whole_blocks_and_noalloc(u):
+    """The budget reserves whole blocks, up to the capacity's need; the no-alloc entry point recomputes dQ."""
     sl, hc, hkv, P = 1024, 8, 4, 4
     h = u.ulysses_create(sl, 1, hc, hkv, 128, P, True, None, torch.bfloat16)
     base = u.ulysses_workspace_size(h)
-    need = 32768 + hc * blocks_per_head(sl, True, None) * 65536
-    u.ulysses_set_ds_budget(h, need - 1)
-    assert u.ulysses_ds_bytes(h) == 0 and u.ulysses_workspace_size(h) == base
-    u.ulysses_set_ds_budget(h, need)
-    assert u.ulysses_ds_bytes(h) == need
-    assert u.ulysses_workspace_size(h) == (base + 1023) // 1024 * 1024 + need
-    u.ulysses_set_ds_budget(h, 0)
-    assert u.ulysses_workspace_size(h) == base
+    rounded = (base + 1023) // 1024 * 1024
+    nblk = blocks_per_head(sl, True, None)
+    need = 32768 + hc * nblk * 65536
+    assert u.ulysses_ds_bytes(h) == (need, 0)
+    for budget, blocks in ((need - 1, nblk - 1), (need, nblk), (need + 10 * hc * 65536, nblk),
+                           (32768 + hc * 65536 - 1, 0), (0, 0)):
+        u.ulysses_set_ds_budget(h, budget)
+        reserved = 32768 + hc * blocks * 65536 if blocks else 0
+        assert u.ulysses_ds_bytes(h) == (need, reserved), budget
+        assert u.ulysses_workspace_size(h) == (rounded + reserved if blocks else base), budget
     h.destroy()
 
     x = random_inputs(sl, 1, hc, hkv, 128, torch.bfloat16, 48)
@@ -137,21 +140,39 @@ def test_budget_threshold_and_noalloc(u):
     assert torch.equal(cat_cpu(dq), ref["dq"])     # the recomputing dQ, bit for bit
 
 
-def test_varying_length_with_stored_ds(u):
-    """One capacity-sized area serves shorter sequences; results match a fixed handle bit for bit."""
+def test_varying_length_with_a_partial_area(u):
+    """An area that holds one 2048-token document: sequences that fit store dS, the others recompute dQ.
+
+    Every set_seq and layer call is enqueued before anything synchronises.
+    Each result equals, bit for bit, a fixed handle's on the same path.
+    """
     hc, hkv, P, cap = 8, 4, 4, 4096
-    V = u.UlyssesLayer.variable_length(cap, 1, hc, hkv, 128, P, True, max_docs=4, ds_budget=BIG)
-    assert V.stores_ds
+    budget = 32768 + hc * blocks_per_head(2048, True, None) * 65536
+    V = u.UlyssesLayer.variable_length(cap, 1, hc, hkv, 128, P, True, max_docs=4, ds_budget=budget)
     ws0 = u.ulysses_workspace_size(V.h)
+    seqs = [(2048, [0, 512, 2048], True), (4096, None, False), (1024, [0, 1, 1024], True),
+            (3072, [0, 1024, 2048, 3072], True), (3072, None, False)]   # three 1024 documents fit; 3072 does not
     outs = []
-    for i, (sl, offs) in enumerate([(2048, [0, 512, 2048]), (4096, None), (1024, [0, 1, 1024])]):
+    for i, (sl, offs, fits) in enumerate(seqs):
         x = random_inputs(sl, 1, hc, hkv, 128, torch.bfloat16, 60 + i)
         V.set_seq(sl, offs)
-        outs.append((sl, offs, x, run(V, x, P)))
+        assert V.stores_ds == fits, (sl, offs)
+        outs.append((sl, offs, fits, x, run(V, x, P)))
     assert u.ulysses_get_status(V.h) == u.ULYSSES_OK
     assert u.ulysses_workspace_size(V.h) == ws0
-    for sl, offs, x, got in outs:
-        F = u.UlyssesLayer(sl, 1, hc, hkv, 128, P, True, offs, torch.bfloat16, ds_budget=BIG)
+    for sl, offs, fits, x, got in outs:
+        F = u.UlyssesLayer(sl, 1, hc, hkv, 128, P, True, offs, torch.bfloat16, ds_budget=BIG if fits else 0)
+        assert F.stores_ds == fits
         ref = run(F, x, P)
         for n in ("o", "dq", "dk", "dv"):
             assert torch.equal(got[n], ref[n]), (sl, n)
+    sl, offs, _, x, got = outs[1]                 # the recomputed one, against the oracle
+    qs, ks, vs, dos = (oracle.shard_sequence(x[n], P) for n in ("q", "k", "v", "do"))
+    g = oracle.ulysses_backward(qs, ks, vs, dos, P, causal=True, doc_offsets=offs)
+    assert_close("dq recomputed in a partial area", got["dq"], oracle.unshard_sequence(g["dq"]), torch.bfloat16)
+
+
+def test_default_budget_of_a_fixed_layer_is_its_own_need(u):
+    L = u.UlyssesLayer(2048, 1, 8, 4, 128, 4, True, [0, 700, 2048], torch.bfloat16)
+    need, reserved = u.ulysses_ds_bytes(L.h)
+    assert L.stores_ds and need == reserved == 32768 + 8 * blocks_per_head(2048, True, [0, 700, 2048]) * 65536

@@ -110,7 +110,7 @@ def test_null_handle_calls_are_rejected(u):
     assert lib.ulysses_timing_enable(None, 1) == u.ULYSSES_ERR_INVALID_ARG
     assert lib.ulysses_timing_read(None, 0, None, None) == u.ULYSSES_ERR_INVALID_ARG
     assert lib.ulysses_set_ds_budget(None, 1 << 30) == u.ULYSSES_ERR_INVALID_ARG
-    assert lib.ulysses_ds_bytes(None, ctypes.byref(n)) == u.ULYSSES_ERR_INVALID_ARG
+    assert lib.ulysses_ds_bytes(None, ctypes.byref(n), None) == u.ULYSSES_ERR_INVALID_ARG
     lib.ulysses_destroy(None)
 
 

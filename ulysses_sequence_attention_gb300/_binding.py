@@ -69,7 +69,7 @@ lib.ulysses_workspace_size.argtypes = [_vp, ctypes.POINTER(ctypes.c_size_t)]
 lib.ulysses_workspace_size.restype = ctypes.c_int
 lib.ulysses_set_ds_budget.argtypes = [_vp, ctypes.c_size_t]
 lib.ulysses_set_ds_budget.restype = ctypes.c_int
-lib.ulysses_ds_bytes.argtypes = [_vp, ctypes.POINTER(ctypes.c_size_t)]
+lib.ulysses_ds_bytes.argtypes = [_vp, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)]
 lib.ulysses_ds_bytes.restype = ctypes.c_int
 lib.ulysses_seq_to_head.argtypes = [_vp, ctypes.c_int, _pp, _pp, _vp]
 lib.ulysses_seq_to_head.restype = ctypes.c_int
@@ -214,10 +214,11 @@ def ulysses_set_ds_budget(h: UlyssesHandle, nbytes: int):
     _check(lib.ulysses_set_ds_budget(h.ptr, int(nbytes)), "ulysses_set_ds_budget")
 
 
-def ulysses_ds_bytes(h: UlyssesHandle) -> int:
-    n = ctypes.c_size_t()
-    _check(lib.ulysses_ds_bytes(h.ptr, ctypes.byref(n)), "ulysses_ds_bytes")
-    return int(n.value)
+def ulysses_ds_bytes(h: UlyssesHandle):
+    """(needed, reserved): the stored-dS area the current sequence uses, and the one reserved."""
+    n, r = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib.ulysses_ds_bytes(h.ptr, ctypes.byref(n), ctypes.byref(r)), "ulysses_ds_bytes")
+    return int(n.value), int(r.value)
 
 
 def _stream(stream):

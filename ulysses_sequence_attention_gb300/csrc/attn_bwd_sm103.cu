@@ -1282,7 +1282,7 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
   const long long nrows = (long long)L.bs * L.Hq;
   const long long per_rank = 2 * nrows * pitch;
   // Stored dS: the zero block, then the blocks of every (rank, batch, head).
-  store_ds = store_ds && L.ds_on;
+  store_ds = store_ds && L.ds_fits();
   char* ds_zero = store_ds ? reinterpret_cast<char*>(workspace) + bwd_ds_offset(L) : nullptr;
   char* ds = store_ds ? ds_zero + dkdv::kDSBlock : nullptr;
   const size_t ds_per_rank = (size_t)L.bs * L.Hq * (size_t)L.ds_nblk * 2 * dkdv::kDSBlock;

@@ -9,6 +9,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <type_traits>
 #include <new>
@@ -239,23 +240,28 @@ void ulysses_destroy(ulysses_t h) {
 int ulysses_workspace_size(ulysses_t h, size_t* bytes) {
   const Layer* L = reinterpret_cast<const Layer*>(h);
   if (!L || !bytes) return ULYSSES_ERR_INVALID_ARG;
-  *bytes = uly::workspace_bytes(*L, L->ds_on);
+  *bytes = uly::workspace_bytes(*L, true);
   return ULYSSES_OK;
 }
 
 int ulysses_set_ds_budget(ulysses_t h, size_t bytes) {
   Layer* L = reinterpret_cast<Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
-  L->ds_budget = bytes;
-  const int64_t nblk = uly::ds_blocks_at_capacity(*L);
-  L->ds_on = nblk > 0 && uly::bwd_ds_bytes(*L, nblk) <= bytes;
+  // As many blocks per (rank, batch, head) as the budget holds, and no more
+  // than one document at capacity needs.
+  const int64_t cap = uly::ds_blocks_at_capacity(*L);
+  const size_t zero = uly::bwd_ds_bytes(*L, 0), per = uly::bwd_ds_bytes(*L, 1) - zero;
+  const int64_t fit = bytes > zero ? (int64_t)std::min<size_t>((bytes - zero) / per, (size_t)cap) : 0;
+  L->ds_reserved = cap > 0 ? fit : 0;
   return ULYSSES_OK;
 }
 
-int ulysses_ds_bytes(ulysses_t h, size_t* bytes) {
+int ulysses_ds_bytes(ulysses_t h, size_t* needed, size_t* reserved) {
   const Layer* L = reinterpret_cast<const Layer*>(h);
-  if (!L || !bytes) return ULYSSES_ERR_INVALID_ARG;
-  *bytes = L->ds_on ? uly::bwd_ds_bytes(*L, uly::ds_blocks_at_capacity(*L)) : 0;
+  if (!L) return ULYSSES_ERR_INVALID_ARG;
+  const bool tc = uly::ds_blocks_at_capacity(*L) > 0;
+  if (needed) *needed = tc && L->ds_nblk > 0 ? uly::bwd_ds_bytes(*L, L->ds_nblk) : 0;
+  if (reserved) *reserved = L->ds_reserved > 0 ? uly::bwd_ds_bytes(*L, L->ds_reserved) : 0;
   return ULYSSES_OK;
 }
 
@@ -357,8 +363,8 @@ size_t workspace_bytes(const Layer& L, bool with_ds) {
   cap.hs = L.hs;
   cap.dtype = L.dtype;
   if (!fwd_sm103_supported(cap)) return (size_t)cap.P * cap.bs * cap.Hq * cap.sl * sizeof(float);
-  if (!with_ds) return bwd_sm103_workspace(cap);
-  return bwd_ds_offset(L) + bwd_ds_bytes(L, ds_blocks_at_capacity(L));
+  if (!with_ds || L.ds_reserved <= 0) return bwd_sm103_workspace(cap);
+  return bwd_ds_offset(L) + bwd_ds_bytes(L, L.ds_reserved);
 }
 
 // Stored-dS blocks per (rank, batch, head) of the longest sequence the handle

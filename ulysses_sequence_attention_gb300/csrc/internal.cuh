@@ -139,11 +139,13 @@ struct Layer {
   // workspace, and dQ = s dS K reads it back instead of recomputing S and dP.
   // Per 256-key pair tile, the index of its first block within a (rank,
   // batch, head); ds_nblk blocks per (rank, batch, head) for the current
-  // sequence. On when the capacity's dS fits the budget.
+  // sequence. The workspace reserves ds_reserved blocks per (rank, batch,
+  // head) (ulysses_set_ds_budget); a backward stores dS when the current
+  // sequence's ds_nblk fit.
   int* d_ds_base = nullptr;
   int64_t ds_nblk = 0;
-  size_t ds_budget = 0;
-  bool ds_on = false;
+  int64_t ds_reserved = 0;
+  bool ds_fits() const { return ds_reserved > 0 && ds_nblk > 0 && ds_nblk <= ds_reserved; }
   long long timeout_cycles = 4000000000LL;  // bound of every device-side wait (~2 s)
   mutable int inject_fault = 0;             // test hook (ulysses_inject_fault), consumed by one call
   mutable Timing timing;                    // ulysses_timing_enable / ulysses_timing_read
@@ -229,7 +231,8 @@ size_t bwd_sm103_workspace(const Layer& L);
 size_t bwd_ds_bytes(const Layer& L, int64_t nblk);
 size_t bwd_ds_offset(const Layer& L);
 // fused: q, k, v, o, dO, dq, dk, dv are sequence shards (else head shards).
-// store_ds: the workspace holds the stored-dS area (L.ds_on) and may use it.
+// store_ds: the workspace holds the reserved stored-dS area and may use it
+// (dS is stored when the current sequence fits it, L.ds_fits()).
 int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* const* k, const void* const* v,
                           const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,
                           void* const* dk, void* const* dv, void* workspace, cudaStream_t s, bool fused = false,
@@ -258,7 +261,8 @@ struct PerDeviceOnce {
 };
 
 // Workspace of the backward for the handle's capacity, with or without the
-// stored-dS area; the blocks per (rank, batch, head) at capacity.
+// reserved stored-dS area; the blocks per (rank, batch, head) of one
+// document at capacity (the most any sequence of the handle needs).
 size_t workspace_bytes(const Layer& L, bool with_ds);
 int64_t ds_blocks_at_capacity(const Layer& L);
 // ulysses_attn_bwd; store_ds = false keeps to the row planes of the workspace

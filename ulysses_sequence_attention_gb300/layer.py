@@ -19,10 +19,10 @@ Two ways to run them, both through the C-ABI of libulysses.so:
 Both give bit-identical results. This class only owns the intermediate buffers
 (torch device memory) and enqueues the calls on the current stream.
 
-The backward's workspace also holds dS when the whole dS of the layer's
-capacity fits its dS budget (ulysses_set_ds_budget; by default up to 64 GiB
-and a quarter of the device): the dK/dV kernel writes it and dQ reads it
-back, instead of recomputing S and dP.
+The backward's workspace can also hold dS (ulysses_set_ds_budget; by default
+up to 64 GiB and a quarter of the device): the dK/dV kernel writes it and dQ
+reads it back, instead of recomputing S and dP, for every sequence whose dS
+fits the reserved area.
 
 HostSteps runs whole training steps from host memory (ulysses_host_*): inputs
 in, forward and backward, outputs out, with the copies overlapped with the
@@ -57,13 +57,19 @@ class UlyssesLayer:
                  _handle=None):
         """fused: None picks the fused path when the shape allows it; True requires it.
 
-        ds_budget: bytes the backward may keep dS in (ulysses_set_ds_budget);
-        None = default_ds_budget(device). dQ then reads dS back instead of
-        recomputing it, when the whole dS of the capacity fits.
+        ds_budget: bytes of workspace the backward may keep dS in
+        (ulysses_set_ds_budget); dQ then reads dS back instead of
+        recomputing it, for every sequence whose dS fits. None: a layer of
+        fixed length reserves what its own sequence needs, if that is within
+        default_ds_budget(device), else nothing; a variable-length layer
+        reserves up to default_ds_budget(device).
         """
         self.h = _handle or B.ulysses_create(sl, bs, hc, hkv, hs, P, causal, doc_offsets, dtype)
-        B.ulysses_set_ds_budget(self.h, default_ds_budget(device) if ds_budget is None else int(ds_budget))
-        self.stores_ds = B.ulysses_ds_bytes(self.h) > 0
+        if ds_budget is None:
+            cap = default_ds_budget(device)
+            need = B.ulysses_ds_bytes(self.h)[0]
+            ds_budget = cap if _handle is not None else (need if need <= cap else 0)
+        B.ulysses_set_ds_budget(self.h, int(ds_budget))
         self.cap_sl = getattr(self.h, "max_sl", sl)
         self.sl, self.bs, self.hc, self.hkv, self.hs, self.P = sl, bs, hc, hkv, hs, P
         self.dtype = dtype
@@ -92,6 +98,12 @@ class UlyssesLayer:
         self.sl = sl
         self._saved = None
         self._pick_path()
+
+    @property
+    def stores_ds(self) -> bool:
+        """Whether the backward of the current sequence keeps dS (its blocks fit the reserved area)."""
+        need, reserved = B.ulysses_ds_bytes(self.h)
+        return 0 < need <= reserved
 
     def _pick_path(self):
         can = B.ulysses_fused_supported(self.h)
