@@ -76,7 +76,8 @@ def exchange_bytes(w, H):
 
 
 KERNEL_SOURCES = {
-    "attn_bwd_dkdv_kernel": "ulysses_sequence_attention_gb300/csrc/attn_bwd_sm103.cu",
+    "attn_bwd_dkdv_kernel<0>": "ulysses_sequence_attention_gb300/csrc/attn_bwd_sm103.cu",
+    "attn_bwd_dkdv_kernel<1>": "ulysses_sequence_attention_gb300/csrc/attn_bwd_sm103.cu",
     "attn_bwd_dq_kernel": "ulysses_sequence_attention_gb300/csrc/attn_bwd_sm103.cu",
     "attn_bwd_dq_stored_kernel": "ulysses_sequence_attention_gb300/csrc/attn_bwd_sm103.cu",
     "attn_fwd_sm103_kernel": "ulysses_sequence_attention_gb300/csrc/attn_fwd_sm103.cu",
@@ -104,7 +105,8 @@ def kernel_work(w, offs, ds_bytes=0):
           else ("attn_bwd_dq_kernel", "tensor", 1 * fl2, "flop"))
     return {
         "attn_fwd": ("attn_fwd_sm103_kernel", "tensor", 2 * fl2, "flop"),
-        "bwd_dkdv": ("attn_bwd_dkdv_kernel", "tensor", 4 * fl2, "flop"),
+        # <1>: the instantiation that also writes dS
+        "bwd_dkdv": ("attn_bwd_dkdv_kernel<1>" if ds_bytes else "attn_bwd_dkdv_kernel<0>", "tensor", 4 * fl2, "flop"),
         "bwd_dq": dq,
         "bwd_prep": ("attn_bwd_prep_kernel", "hbm", tok * w.hc * (2 * w.hs * eb + 4), "byte"),
         "seq_to_head": ("seq_to_head_kernel", "hbm",
