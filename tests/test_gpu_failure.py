@@ -59,11 +59,19 @@ def test_wait_limit_and_fault_kind_are_validated(u):
     h.destroy()
 
 
-def test_backward_timeout_is_reported_and_the_context_survives(u):
-    """Kind 2: the next backward's dK/dV producer issues no Q/dO loads; its waits run out."""
+@pytest.mark.parametrize("ds_budget", [None, 0], ids=["stored_ds", "recomputed_dq"])
+def test_backward_timeout_is_reported_and_the_context_survives(u, ds_budget):
+    """Kind 2: the next backward's dK/dV producer issues no Q/dO loads; its waits run out.
+
+    Both backward paths: with stored dS the dS store thread's wait runs out
+    too (the compute warps never stage a tile), and the dQ kernel then reads
+    whatever the workspace holds; the status word reports the timeout either
+    way, and the next call is right.
+    """
     sl, hc, hkv, P = 256, 2, 1, 1          # one CTA pair, two query tiles per query head
     x = random_inputs(sl, 1, hc, hkv, 128, torch.bfloat16, 42)
-    L = u.UlyssesLayer(sl, 1, hc, hkv, 128, P, True, None, torch.bfloat16)
+    L = u.UlyssesLayer(sl, 1, hc, hkv, 128, P, True, None, torch.bfloat16, ds_budget=ds_budget)
+    assert L.stores_ds == (ds_budget is None)
     cu = lambda t: [s.cuda() for s in split_shards(t, P)]  # noqa: E731
     q, k, v, do = cu(x["q"]), cu(x["k"]), cu(x["v"]), cu(x["do"])
     o = L.new_seq_shards(hc)
