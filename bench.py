@@ -619,6 +619,8 @@ def main():
                                 {"how": "recomputed: the dQ kernel forms S, P, dP and dS again"}),
                 "attention": {"fwd_ms": attn_fwd_ms, "fwd_tflops": fwd_tf, "fwd_frac_sustained": fwd_tf / sustained,
                               "bwd_ms": attn_bwd_ms, "bwd_tflops": bwd_tf,
+                              # 4 GEMMs (2.0x the forward): the figure without recomputing S
+                              "bwd_tflops_no_recompute": (0.8 * bwd_tf) if bwd_tf else None,
                               "bwd_frac_sustained": (bwd_tf / sustained) if bwd_tf else None,
                               "fwd_tflop": fl_fwd / 1e12, "bwd_tflop": fl_bwd / 1e12,
                               "kernel_times": "per-kernel CUDA events: forward kernel; backward prep + dK/dV + dQ",
