@@ -1089,38 +1089,35 @@ struct PrepParams {
   int fused, n;
 };
 
-// A block takes kPrepRows consecutive rows t of one (rank, batch, head): t is
-// the fastest index, so the LSE reads and the row-plane writes are
-// contiguous. Warp w takes rows [8w, 8w+8) of the block in four steps of two
-// rows, a half-warp (16 lanes x 16 bytes of O and of dO) per row, with all
-// eight loads of a lane issued before the first sum. grid.x covers t,
-// grid.y the (rank, batch, head) triples (strided past 65535).
+// Rows are taken in the memory order of the buffers that hold O and dO, so
+// every block streams 64 consecutive 256-byte rows (16 KB) of each: buffer i
+// holds rows rho = (t*bs + b)*Hq + hq of head shard i, or, fused, rows
+// rho = (tt*bs + b)*hc + h of sequence shard i (token t = i*n + tt, rank
+// h / Hq, head h % Hq). Both have sl*bs*Hq rows. Warp w takes rows
+// [8w, 8w+8) of the block in four steps of two rows, a half-warp (16 lanes
+// x 16 bytes of O and of dO) per row, with all eight loads of a lane issued
+// before the first sum. grid.x covers the rows of a buffer, grid.y the
+// buffers.
 constexpr int kPrepRows = 64;
 __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constant__ PrepParams a) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int half = lane >> 4, part = lane & 15;
-  const int t0 = blockIdx.x * kPrepRows + warp * 8;
+  const int src = blockIdx.y;
+  const long long nrows = (long long)a.sl * a.bs * a.Hq;
+  const long long rho0 = (long long)blockIdx.x * kPrepRows + warp * 8;
   if (a.zero && blockIdx.x == 0 && blockIdx.y == 0) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) a.zero[i * 256 + threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
   }
-  const long long triples = (long long)a.P * a.bs * a.Hq;
-  for (long long y = blockIdx.y; y < triples; y += gridDim.y) {
-    const int hq = (int)(y % a.Hq), b = (int)((y / a.Hq) % a.bs), r = (int)(y / ((long long)a.Hq * a.bs));
+  {
     uint4 ov[4], dv[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int t = t0 + 2 * u + half;
+      const long long rho = rho0 + 2 * u + half;
       ov[u] = dv[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (t < a.sl) {
-        int src = r;
-        size_t at = ((size_t)t * a.bs + b) * a.Hq + hq;  // head shard: row (t, b, hq)
-        if (a.fused) {  // sequence shard t / n: row (t - s n, b, r Hq + hq)
-          src = t / a.n;
-          at = ((size_t)(t - src * a.n) * a.bs + b) * (size_t)(a.P * a.Hq) + (size_t)r * a.Hq + hq;
-        }
-        ov[u] = __ldg(reinterpret_cast<const uint4*>(a.o[src] + at * 128) + part);
-        dv[u] = __ldg(reinterpret_cast<const uint4*>(a.dO[src] + at * 128) + part);
+      if (rho < nrows) {
+        ov[u] = __ldg(reinterpret_cast<const uint4*>(a.o[src] + rho * 128) + part);
+        dv[u] = __ldg(reinterpret_cast<const uint4*>(a.dO[src] + rho * 128) + part);
       }
     }
     float acc[4];
@@ -1147,13 +1144,29 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const __grid_constan
       if (lane == 2 * u) d = v0;
       if (lane == 2 * u + 1) d = v1;
     }
-    const size_t row = ((size_t)b * a.Hq + hq) * a.pitch + t0;
-    if (lane < 8) {
-      if (t0 + lane < a.sl) a.rows[r][(size_t)a.bs * a.Hq * a.pitch + row + lane] = d;
-    } else if (lane < 16) {
-      const int j = lane - 8;
-      if (t0 + j < a.sl)
-        a.rows[r][row + j] = -(a.lse[r][((size_t)b * a.Hq + hq) * a.sl + t0 + j] * 1.4426950408889634f);
+    // Lanes 0-7 write D of rows rho0 + lane, lanes 8-15 the -LSE log2(e) of
+    // rows rho0 + lane - 8.
+    const long long rho = rho0 + (lane & 7);
+    if (lane < 16 && rho < nrows) {
+      int t, b, r, hq;
+      if (a.fused) {
+        const int hc = a.P * a.Hq;
+        const int h = (int)(rho % hc);
+        b = (int)((rho / hc) % a.bs);
+        t = src * a.n + (int)(rho / ((long long)hc * a.bs));
+        r = h / a.Hq;
+        hq = h % a.Hq;
+      } else {
+        hq = (int)(rho % a.Hq);
+        b = (int)((rho / a.Hq) % a.bs);
+        t = (int)(rho / ((long long)a.Hq * a.bs));
+        r = src;
+      }
+      const size_t row = ((size_t)b * a.Hq + hq) * a.pitch + t;
+      if (lane < 8)
+        a.rows[r][(size_t)a.bs * a.Hq * a.pitch + row] = d;
+      else
+        a.rows[r][row] = -(a.lse[r][((size_t)b * a.Hq + hq) * a.sl + t] * 1.4426950408889634f);
     }
   }
 }
@@ -1305,8 +1318,8 @@ int launch_attn_bwd_sm103(const Layer& L, const void* const* q, const void* cons
     a.n = (int)L.n();
     a.zero = reinterpret_cast<uint4*>(ds_zero);
     Timed t(L.timing, ULYSSES_KERNEL_BWD_PREP, stream);
-    const long long triples = (long long)L.P * L.bs * L.Hq;
-    const dim3 grid((unsigned)((L.sl + kPrepRows - 1) / kPrepRows), (unsigned)std::min(triples, 65535LL));
+    const long long prep_rows = (long long)L.sl * L.bs * L.Hq;  // rows of each O / dO buffer
+    const dim3 grid((unsigned)((prep_rows + kPrepRows - 1) / kPrepRows), (unsigned)L.P);
     attn_bwd_prep_kernel<<<grid, 256, 0, stream>>>(a);
     t.done();
     count_launches(1);
