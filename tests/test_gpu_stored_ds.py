@@ -172,6 +172,27 @@ def test_varying_length_with_a_partial_area(u):
     assert_close("dq recomputed in a partial area", got["dq"], oracle.unshard_sequence(g["dq"]), torch.bfloat16)
 
 
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("budget", [BIG, 0])
+def test_backward_repeats_bit_for_bit(u, fused, budget):
+    """Five backwards of one packed layer give the same dQ, dK and dV, bit for bit.
+
+    The kernels have no atomics and a fixed order of every sum, so any
+    difference between repetitions is a race (a buffer read before it is
+    written, or overwritten while still in use).
+    """
+    sl, hc, hkv, P, offs = 3072, 32, 8, 8, [0, 57, 1100, 1101, 2900, 3072]
+    x = random_inputs(sl, 1, hc, hkv, 128, torch.bfloat16, 47)
+    L = u.UlyssesLayer(sl, 1, hc, hkv, 128, P, True, offs, torch.bfloat16, fused=fused, ds_budget=budget)
+    assert L.stores_ds == (budget > 0)
+    first = run(L, x, P)
+    for rep in range(4):
+        again = run(L, x, P)
+        for n in ("o", "dq", "dk", "dv"):
+            assert torch.equal(again[n], first[n]), (rep, n)
+    assert u.ulysses_get_status(L.h) == u.ULYSSES_OK
+
+
 def test_default_budget_of_a_fixed_layer_is_its_own_need(u):
     L = u.UlyssesLayer(2048, 1, 8, 4, 128, 4, True, [0, 700, 2048], torch.bfloat16)
     need, reserved = u.ulysses_ds_bytes(L.h)

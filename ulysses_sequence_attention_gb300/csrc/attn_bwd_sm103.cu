@@ -454,7 +454,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t pf[64];
       tmem_ld32(tmem + lane_base + 0 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pf[0]));
       tmem_ld32(tmem + lane_base + 32 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pf[32]));
-      tmem_ld_wait();
+      tmem_ld_wait(pf);
       tc_fence_before();
       warp_arrive_leader(bar(B_SFREE), crank);  // S^T may be overwritten by S of tile it+2
       const float* rs = rows + rsl * 256;
@@ -495,7 +495,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t dp[64];
       tmem_ld32(tmem + lane_base + 128 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
       tmem_ld32(tmem + lane_base + 160 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
-      tmem_ld_wait();
+      tmem_ld_wait(dp);
       // dS^T = P^T * (dP^T - D)
       const uint64_t* d2 = reinterpret_cast<const uint64_t*>(rs + 128 + 64 * h);
       uint32_t dk[32];
@@ -531,7 +531,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t o[64], w[32];
         tmem_ld32(tmem + lane_base + col, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
         tmem_ld32(tmem + lane_base + col + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-        tmem_ld_wait();
+        tmem_ld_wait(o);
 #pragma unroll
         for (int c = 0; c < 32; ++c)
           w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * mul, __uint_as_float(o[2 * c + 1]) * mul);
@@ -795,7 +795,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t pf[64];
       tmem_ld32(tmem + lane_base + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pf[0]));
       tmem_ld32(tmem + lane_base + 32 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pf[32]));
-      tmem_ld_wait();
+      tmem_ld_wait(pf);
       tc_fence_before();
       warp_arrive_cluster(sfree_c);  // S may be overwritten by S of tile jj+1
       const bool full = klo <= k0 && k0 + 63 <= khi;
@@ -817,7 +817,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t dp[64];
       tmem_ld32(dpb, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
       tmem_ld32(dpb + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
-      tmem_ld_wait();
+      tmem_ld_wait(dp);
       uint32_t dk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) dk[c] = f2_pack_bf16(f2_mul(pp[c], f2_sub(f2_bits(dp[2 * c], dp[2 * c + 1]), D2)));
@@ -834,7 +834,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t o[64], w[32];
       tmem_ld32(tmem + lane_base + 384 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
       tmem_ld32(tmem + lane_base + 416 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-      tmem_ld_wait();
+      tmem_ld_wait(o);
 #pragma unroll
       for (int c = 0; c < 32; ++c)
         w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * p.scale, __uint_as_float(o[2 * c + 1]) * p.scale);
@@ -1041,7 +1041,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(dqs::kThreads, 1)
         uint32_t o[64], w[32];
         tmem_ld32(tmem + lane_base + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
         tmem_ld32(tmem + lane_base + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
-        tmem_ld_wait();
+        tmem_ld_wait(o);
 #pragma unroll
         for (int c = 0; c < 32; ++c)
           w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * p.scale, __uint_as_float(o[2 * c + 1]) * p.scale);

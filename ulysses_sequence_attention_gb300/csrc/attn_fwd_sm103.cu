@@ -299,7 +299,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
         tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
         tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-        tmem_ld_wait();
+        tmem_ld_wait(s);
         const int kb = (kr.x + jj) * 128;
         if (!(lo <= kb && kb + 127 <= hi)) {
 #pragma unroll
@@ -331,7 +331,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int q = 0; q < 4; ++q) {
             uint32_t o[32];
             tmem_ld32(t_o + 32 * q, o);
-            tmem_ld_wait();
+            tmem_ld_wait(o);
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
               float lo2, hi2;
@@ -374,7 +374,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 4; ++q) {
           uint32_t o[32];
           tmem_ld32(t_o + 32 * q, o);
-          tmem_ld_wait();
+          tmem_ld_wait(o);
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             uint32_t w[4];
