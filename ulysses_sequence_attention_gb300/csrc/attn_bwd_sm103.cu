@@ -214,6 +214,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const long long lim = p.timeout;
+  // The stored-dS instantiation waits with one polling lane per warp
+  // (warp_wait); with every lane polling, its dS was in some builds formed
+  // from stale values. The other keeps every lane polling, which is faster.
+  auto dkdv_wait = [&](uint32_t b_, uint32_t parity) {
+    if constexpr (kStore)
+      return warp_wait(b_, parity, lim);
+    else
+      return __all_sync(0xffffffffu, mbar_wait(b_, parity, lim));
+  };
 
   if (warp >= 8) {
     regs_dec<kRegsOther>();
@@ -243,7 +252,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int q0 = (qr.x + it % nm) * 128;
           const uint32_t sq = sb + kOffStage + st * kStage;
           // query-half part: Q and dO rows [q0 + 64c, +64) (B of S^T, dP^T: N = queries)
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_QEMPTY + st), (u & 1) ^ 1, lim));
+          ok = dkdv_wait(bar(B_QEMPTY + st), (u & 1) ^ 1);
           if (!ok) break;
           if (lane == 0 && !p.skip_q_loads) {
             const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hq, hq, q0);
@@ -260,7 +269,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // done. Rows past sl read as zero; every key masks them, so P = 0
           // there and dS = 0.
           const int rsl = it % NR;
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_REMPTY + rsl), ((it / NR) & 1) ^ 1, lim));
+          ok = dkdv_wait(bar(B_REMPTY + rsl), ((it / NR) & 1) ^ 1);
           if (!ok) break;
           if (lane == 0) {
             mbar_expect_tx(bar(B_RFULL + rsl), 1024);
@@ -274,7 +283,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int hq = hk * p.group + ih / nm;
           const int q0 = (qr.x + ih % nm) * 128;
           const uint32_t sq = sb + kOffStage + st * kStage;
-          ok = __all_sync(0xffffffffu, mbar_wait(bar(B_HEMPTY + st), (u & 1) ^ 1, lim));
+          ok = dkdv_wait(bar(B_HEMPTY + st), (u & 1) ^ 1);
           if (!ok) break;
           if (lane == 0 && !p.skip_q_loads) {
             const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hq, hq, q0);
@@ -447,8 +456,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int it = 0; it < n_it; ++it) {
       const int m = qr.x + it % nm;
       const int rsl = it % NR;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_S), it & 1, lim) &&
-                                       mbar_wait(bar(B_RFULL + rsl), (it / NR) & 1, lim));
+      ok = dkdv_wait(bar(B_S), it & 1);
+      ok = ok && dkdv_wait(bar(B_RFULL + rsl), (it / NR) & 1);
       if (!ok) break;
       tc_fence_after();
       uint32_t pf[64];
@@ -480,7 +489,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) pk[c] = f2_pack_bf16(pp[c]);
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DP), it & 1, lim));
+      ok = dkdv_wait(bar(B_DP), it & 1);
       if (!ok) break;
       tc_fence_after();
       if (warp == 0 && lane == 0) {
@@ -512,14 +521,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (kStore) {
         // dS^T row jr = column jr of dS, staged for the store thread once it
         // has read the previous tile's image out.
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DSFREE), (it & 1) ^ 1, lim));
+        ok = dkdv_wait(bar(B_DSFREE), (it & 1) ^ 1);
         if (!ok) break;
         stage_row64(sb + kOffDS + h * kHalf, jr, dk);
         fence_proxy_async_smem();
         warp_arrive_local(bar(B_DSFULL));
       }
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DONE), 0, lim));
+    if (ok) ok = dkdv_wait(bar(B_DONE), 0);
     if (ok) {
       tc_fence_after();
       // dV (columns 256+) and dK (384+, times s) of key row jr, head-dimension

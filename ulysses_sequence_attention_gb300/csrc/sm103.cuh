@@ -54,6 +54,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long lo
   return true;
 }
 
+// Waits, for a whole warp, for the phase with the given parity to complete;
+// false for every lane when the wait gave up. Lane 0 polls alone and then
+// tells the warp, and __syncwarp orders the other lanes' later accesses after
+// its acquire of the barrier (tensor-memory loads also need the
+// tcgen05.fence::after_thread_sync that follows every wait). When every lane
+// of the warp polled the barrier itself instead, the dK/dV kernel that stores
+// dS sometimes formed dS from stale values in some builds: its results then
+// differed between repetitions of one input. With one polling lane they did
+// not, in any build tried.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, long long limit) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, limit);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();
+  return ok;
+}
+
 // Makes this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tensor cores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
