@@ -214,15 +214,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const long long lim = p.timeout;
-  // The stored-dS instantiation waits with one polling lane per warp
-  // (warp_wait); with every lane polling, its dS was in some builds formed
-  // from stale values. The other keeps every lane polling, which is faster.
-  auto dkdv_wait = [&](uint32_t b_, uint32_t parity) {
-    if constexpr (kStore)
-      return warp_wait(b_, parity, lim);
-    else
-      return __all_sync(0xffffffffu, mbar_wait(b_, parity, lim));
-  };
 
   if (warp >= 8) {
     regs_dec<kRegsOther>();
@@ -252,7 +243,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int q0 = (qr.x + it % nm) * 128;
           const uint32_t sq = sb + kOffStage + st * kStage;
           // query-half part: Q and dO rows [q0 + 64c, +64) (B of S^T, dP^T: N = queries)
-          ok = dkdv_wait(bar(B_QEMPTY + st), (u & 1) ^ 1);
+          ok = warp_wait(bar(B_QEMPTY + st), (u & 1) ^ 1, lim);
           if (!ok) break;
           if (lane == 0 && !p.skip_q_loads) {
             const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hq, hq, q0);
@@ -269,7 +260,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // done. Rows past sl read as zero; every key masks them, so P = 0
           // there and dS = 0.
           const int rsl = it % NR;
-          ok = dkdv_wait(bar(B_REMPTY + rsl), ((it / NR) & 1) ^ 1);
+          ok = warp_wait(bar(B_REMPTY + rsl), ((it / NR) & 1) ^ 1, lim);
           if (!ok) break;
           if (lane == 0) {
             mbar_expect_tx(bar(B_RFULL + rsl), 1024);
@@ -283,7 +274,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int hq = hk * p.group + ih / nm;
           const int q0 = (qr.x + ih % nm) * 128;
           const uint32_t sq = sb + kOffStage + st * kStage;
-          ok = dkdv_wait(bar(B_HEMPTY + st), (u & 1) ^ 1);
+          ok = warp_wait(bar(B_HEMPTY + st), (u & 1) ^ 1, lim);
           if (!ok) break;
           if (lane == 0 && !p.skip_q_loads) {
             const TileLoc l = locate_tile(p.fused, p.n, p.nranks, rl, p.Hq, hq, q0);
@@ -456,8 +447,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int it = 0; it < n_it; ++it) {
       const int m = qr.x + it % nm;
       const int rsl = it % NR;
-      ok = dkdv_wait(bar(B_S), it & 1);
-      ok = ok && dkdv_wait(bar(B_RFULL + rsl), (it / NR) & 1);
+      ok = warp_wait(bar(B_S), it & 1, lim);
+      ok = ok && warp_wait(bar(B_RFULL + rsl), (it / NR) & 1, lim);
       if (!ok) break;
       tc_fence_after();
       uint32_t pf[64];
@@ -489,7 +480,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) pk[c] = f2_pack_bf16(pp[c]);
-      ok = dkdv_wait(bar(B_DP), it & 1);
+      ok = warp_wait(bar(B_DP), it & 1, lim);
       if (!ok) break;
       tc_fence_after();
       if (warp == 0 && lane == 0) {
@@ -510,7 +501,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t dk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) dk[c] = f2_pack_bf16(f2_mul(pp[c], f2_sub(f2_bits(dp[2 * c], dp[2 * c + 1]), d2[c])));
-      warp_arrive_local(bar(B_REMPTY + rsl));  // done with this tile's LSE/D rows
+      // Done with this tile's LSE/D rows. The producer refills the slot by
+      // TMA (the async proxy) once every warp has arrived: the proxy fence
+      // orders this thread's generic reads of the slot before that write.
+      fence_proxy_async_smem();
+      warp_arrive_local(bar(B_REMPTY + rsl));
       // P^T and dS^T (bf16) over the dP^T columns this thread has just read:
       // no other thread reads them
       tmem_st32(tmem + lane_base + 128 + 64 * h, pk);
@@ -521,14 +516,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (kStore) {
         // dS^T row jr = column jr of dS, staged for the store thread once it
         // has read the previous tile's image out.
-        ok = dkdv_wait(bar(B_DSFREE), (it & 1) ^ 1);
+        ok = warp_wait(bar(B_DSFREE), (it & 1) ^ 1, lim);
         if (!ok) break;
         stage_row64(sb + kOffDS + h * kHalf, jr, dk);
         fence_proxy_async_smem();
         warp_arrive_local(bar(B_DSFULL));
       }
     }
-    if (ok) ok = dkdv_wait(bar(B_DONE), 0);
+    if (ok) ok = warp_wait(bar(B_DONE), 0, lim);
     if (ok) {
       tc_fence_after();
       // dV (columns 256+) and dK (384+, times s) of key row jr, head-dimension
@@ -798,7 +793,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int jj = 0; jj < n_kv; ++jj) {
       const int k0 = (kr.x + jj) * 128 + 64 * h;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DP), jj & 1, lim));
+      ok = warp_wait(bar(B_DP), jj & 1, lim);
       if (!ok) break;
       tc_fence_after();
       uint32_t pf[64];
@@ -835,7 +830,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       warp_arrive_cluster(ds_c);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DONE), 0, lim));
+    if (ok) ok = warp_wait(bar(B_DONE), 0, lim);
     if (ok) {
       tc_fence_after();
       // dQ (times s) of query row iq, head-dimension half h, staged in the Q
@@ -1042,7 +1037,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(dqs::kThreads, 1)
     // is done) as two 64-column halves and TMA-stored.
     const int iq = warp * 32 + lane;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(B_DONE), 0, lim));
+    const bool ok = warp_wait(bar(B_DONE), 0, lim);
     if (ok) {
       tc_fence_after();
 #pragma unroll

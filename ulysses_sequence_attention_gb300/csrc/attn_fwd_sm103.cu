@@ -287,7 +287,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;
       for (int jj = 0; jj < n_kv; ++jj) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_SFULL + t), jj & 1, lim));
+        ok = warp_wait(bar(B_SFULL + t), jj & 1, lim);
         if (!ok) break;
         tc_fence_after();
         // S of the last tile for key tile jj is the last UMMA issued for key
@@ -362,7 +362,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         warp_arrive_leader(bar(B_PFULL + t), crank);
       }
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar(B_OFINAL + t), 0, lim));
+      if (ok) ok = warp_wait(bar(B_OFINAL + t), 0, lim);
       if (ok) {
         tc_fence_after();
         // Normalise O and stage it, 128-byte swizzled, in this tile's Q buffer

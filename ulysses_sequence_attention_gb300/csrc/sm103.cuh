@@ -54,25 +54,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long lo
   return true;
 }
 
-// Waits, for a whole warp, for the phase with the given parity to complete;
-// false for every lane when the wait gave up. Lane 0 polls alone and then
-// tells the warp, and __syncwarp orders the other lanes' later accesses after
-// its acquire of the barrier (tensor-memory loads also need the
-// tcgen05.fence::after_thread_sync that follows every wait). When every lane
-// of the warp polled the barrier itself instead, the dK/dV kernel that stores
-// dS sometimes formed dS from stale values in some builds: its results then
-// differed between repetitions of one input. With one polling lane they did
-// not, in any build tried.
+// The wait of a whole warp: every lane tests the phase in the same
+// instruction, the warp votes, and the loop ends only when the vote says
+// every lane saw the phase complete (or, for every lane at once, when the
+// limit has passed). The loop's exit is warp-uniform, so the warp reaches the
+// warp-collective instructions that follow (.sync.aligned tensor-memory loads
+// and stores, shuffles, warp barriers) converged, and each lane's own
+// successful test is an acquire of the barrier for the data it then reads.
+// Every kernel uses this form for the waits of whole warps; single-thread
+// waits (producers, issuers) use mbar_wait.
+//
+// A lane that already saw the phase complete may test it again. That test
+// stays true: no barrier here completes a second phase before the waiting
+// warp has arrived on what gates that phase (each kernel's barrier list says
+// which arrival it is). Returns false for every lane when it gave up.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, long long limit) {
-  bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, limit);
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  __syncwarp();
-  return ok;
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+  const long long t0 = clock64();
+  while (!__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) {
+    if (__any_sync(0xffffffffu, clock64() - t0 > limit)) return false;
+  }
+  return true;
 }
 
-// Makes this thread's generic-proxy shared-memory writes visible to the async
-// proxy (TMA, tensor cores).
+// Orders this thread's generic-proxy shared-memory accesses before the async
+// proxy's (TMA, tensor cores, bulk copies) that follow a synchronisation:
+// writes that a bulk copy or a UMMA will read, and reads of a buffer that a
+// TMA load will refill. An mbarrier release/acquire alone orders generic
+// accesses only.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
