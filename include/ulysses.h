@@ -505,11 +505,11 @@ int ulysses_timing_read(ulysses_t h, int kernel, double* total_ms, int64_t* laun
  *
  * Arguments and results are those of ulysses_attn_bwd, without `workspace`.
  * The workspace is a file-scope device array of
- * ULYSSES_NOALLOC_SCRATCH_BYTES bytes inside the library. Every GPU that loads
- * the library holds this array until the process exits. This call never
- * calls cudaMalloc, cudaFree or any allocating library routine. The handle
- * still comes from ulysses_create, which allocates a few bytes of metadata:
- * create it during set-up.
+ * ULYSSES_NOALLOC_SCRATCH_BYTES bytes inside the library. Every GPU on which
+ * a handle has been created holds this array until the process exits. This
+ * call never calls cudaMalloc, cudaFree or any allocating library routine.
+ * The handle still comes from ulysses_create, which allocates a few bytes of
+ * metadata and sets up the array (below): create it during set-up.
  *
  * Limits and sharing:
  *  - A layer whose backward needs more than ULYSSES_NOALLOC_SCRATCH_BYTES of
@@ -524,9 +524,15 @@ int ulysses_timing_read(ulysses_t h, int kernel, double* total_ms, int64_t* laun
  *    overlap on the GPU (on different streams, or different host threads
  *    without ordering) race on the array and corrupt each other's gradients:
  *    order them.
- *  - The first call on a device looks up the array's device address with
- *    cudaGetSymbolAddress (once per device, with that device current). Make
- *    that first call before any stream capture begins.
+ *  - The array's device address comes from cudaGetSymbolAddress, looked up
+ *    by ulysses_create (and ulysses_create_varlen) on the current device.
+ *    That lookup loads the array on the device: its 64 MiB are committed
+ *    when the first handle of a device is created, not when the library is
+ *    loaded. A call of this function then allocates nothing. If that lookup
+ *    failed, the first call here tries once more and returns
+ *    ULYSSES_ERR_CUDA if it fails again; make that call before any stream
+ *    capture begins. A cudaDeviceReset destroys the array with every handle
+ *    of the device; handles created after it look the array up again.
  */
 #define ULYSSES_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 int ulysses_attn_bwd_noalloc(ulysses_t h, const void* const* q, const void* const* k,

@@ -76,6 +76,33 @@ def test_noalloc_matches_the_allocating_entry_point(u, sl, hc, hkv, P, offs):
                 assert torch.equal(gs[r], rs[r])
 
 
+def test_noalloc_call_allocates_no_device_memory(u):
+    """A call after set-up leaves the device's free memory and torch's allocator untouched.
+
+    The handle (ulysses_create) sets the scratch array up; the outputs are
+    allocated before the measurement. A first call launches every kernel
+    once (the driver can size per-kernel resources on a first launch); the
+    second is measured.
+    """
+    sl, hc, hkv, P = 1024, 8, 4, 4
+    L, b = _forward(u, sl, hc, hkv, P, seed=32)
+    args = (b["qh"], b["kh"], b["vh"], b["oh"], b["doh"], b["lse"])
+    first, second = _grads(L, None), _grads(L, None)
+    u.ulysses_attn_bwd_noalloc(L.h, *args, *first)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    u.ulysses_attn_bwd_noalloc(L.h, *args, *second)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert u.ulysses_get_status(L.h) == u.ULYSSES_OK
+    assert free1 == free0, f"device free memory changed by {free0 - free1} bytes"
+    assert torch.cuda.memory_allocated() == alloc0
+    for a, c in zip(first, second):
+        for r in range(P):
+            assert torch.equal(a[r], c[r])
+
+
 def test_noalloc_rejects_a_layer_beyond_its_scratch(u):
     # The row planes need 8 bytes per (token, query head, batch element):
     # 256 tokens x 2 heads x 65535 batch = 256 MiB > 64 MiB. The size check

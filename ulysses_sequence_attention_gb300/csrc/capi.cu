@@ -173,6 +173,7 @@ static int create_layer(ulysses_t* out, int64_t sl, int64_t bs, int hc, int hkv,
     free_layer(L);
     return ULYSSES_ERR_CUDA;
   }
+  uly::noalloc_setup();
   *out = reinterpret_cast<ulysses_t>(L);
   return ULYSSES_OK;
 }

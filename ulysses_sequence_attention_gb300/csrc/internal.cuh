@@ -271,6 +271,10 @@ int attn_bwd_entry(ulysses_t h, const void* const* q, const void* const* k, cons
                    const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,
                    void* const* dk, void* const* dv, void* workspace, void* stream, bool store_ds);
 
+// Looks up, and so loads, the no-alloc scratch array on the current device
+// (noalloc.cu); ulysses_create calls it during set-up.
+void noalloc_setup();
+
 // Frees the host-streaming streams and events of a handle (host_step.cu).
 void destroy_host_pipe(Layer& L);
 
