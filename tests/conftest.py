@@ -28,3 +28,18 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """The plain max-abs and mean-abs of every parity comparison of the session."""
+    try:
+        from tests._gpu import RECORDS
+    except Exception:  # pragma: no cover
+        return
+    if not RECORDS:
+        return
+    tr = terminalreporter
+    tr.section("parity against the oracle: max-abs, mean-abs, worst |x-ref|/bound, elements under a derived bound")
+    for test, name, n, mx, mean, worst, derived in RECORDS:
+        tr.write_line(f"{test} | {name} | {n} elements | max-abs {mx:.3g} | mean-abs {mean:.3g} | {worst:.3g} | "
+                      f"{derived}")

@@ -20,7 +20,7 @@ import pytest
 import torch
 
 import oracle
-from tests._gpu import assert_close, cat_cpu
+from tests._gpu import assert_close, cat_cpu, replica_allowance, rounding_sigma
 from workloads import random_inputs, split_shards
 
 pytestmark = pytest.mark.gpu
@@ -96,10 +96,12 @@ def test_stored_ds_against_the_oracle_and_the_recomputing_dq(u, sl, bs, hc, hkv,
 
     qs, ks, vs, dos = (oracle.shard_sequence(x[n], P) for n in ("q", "k", "v", "do"))
     g = oracle.ulysses_backward(qs, ks, vs, dos, P, causal=causal, doc_offsets=offs)
+    sig = rounding_sigma(x, causal, offs)
     for n in ("dq", "dk", "dv"):
         want = oracle.unshard_sequence(g[n])
-        assert_close(f"{n} stored", got[n], want, dt)
-        assert_close(f"{n} recomputed", ref[n], want, dt)
+        extra = replica_allowance(g, n, P, hkv, dt)
+        assert_close(f"{n} stored", got[n], want, dt, extra=extra, sigma=sig.get(n))
+        assert_close(f"{n} recomputed", ref[n], want, dt, extra=extra, sigma=sig.get(n))
 
 
 def test_budget_reserves_whole_blocks_and_noalloc(u):
@@ -175,18 +177,20 @@ def test_varying_length_with_a_partial_area(u):
 @pytest.mark.parametrize("fused", [True, False])
 @pytest.mark.parametrize("budget", [BIG, 0])
 def test_backward_repeats_bit_for_bit(u, fused, budget):
-    """Five backwards of one packed layer give the same dQ, dK and dV, bit for bit.
+    """Twenty backwards of one packed layer give the same dQ, dK and dV, bit for bit.
 
     The kernels have no atomics and a fixed order of every sum, so any
     difference between repetitions is a race (a buffer read before it is
-    written, or overwritten while still in use).
+    written, or overwritten while still in use). This shape (shards of 384
+    tokens, documents of 57 and 1 tokens) is the one on which per-lane
+    polling loops made the stored-dS dK/dV kernel vary.
     """
     sl, hc, hkv, P, offs = 3072, 32, 8, 8, [0, 57, 1100, 1101, 2900, 3072]
     x = random_inputs(sl, 1, hc, hkv, 128, torch.bfloat16, 47)
     L = u.UlyssesLayer(sl, 1, hc, hkv, 128, P, True, offs, torch.bfloat16, fused=fused, ds_budget=budget)
     assert L.stores_ds == (budget > 0)
     first = run(L, x, P)
-    for rep in range(4):
+    for rep in range(19):
         again = run(L, x, P)
         for n in ("o", "dq", "dk", "dv"):
             assert torch.equal(again[n], first[n]), (rep, n)

@@ -99,14 +99,38 @@ def test_replicated_kv_heads():
         assert torch.all(s == P // hkv)
 
 
+@pytest.mark.parametrize("sl,bs,H,hs,P,elem", [(24, 2, 8, 3, 4, 2), (12, 3, 6, 5, 3, 4), (16, 1, 4, 7, 1, 2)])
+def test_exchange_bytes_counts_what_the_exchange_moves(sl, bs, H, hs, P, elem):
+    """exchange_bytes against the oracle's own exchange, block by block.
+
+    An index-encoded tensor tells where every element of every head shard
+    came from. The blocks (source rank s -> destination rank r) add up to the
+    whole tensor once: exchange_bytes. The DeepSpeed-Ulysses blog (section
+    "显著的通信量减少") puts M/P on each GPU's links for an aggregate message
+    M: each of the P^2 blocks holds M/P^2, and each rank sends the (P-1)/P of
+    its M/P that it does not keep. Sizes are all different, so a dropped or
+    repeated factor (batch, head size, element size) fails.
+    """
+    x = encoded(sl, bs, H, hs)
+    n = sl // P
+    head = oracle.seq_to_head(oracle.shard_sequence(x, P), P)
+    block = torch.zeros(P, P, dtype=torch.int64)      # [source, destination] elements
+    for r, shard in enumerate(head):
+        t, _, _, _ = decode(shard)
+        src = (t // n).flatten()
+        block[:, r] += torch.bincount(src, minlength=P)
+    M = oracle.exchange_bytes(sl, bs, H, hs, elem)
+    assert int(block.sum()) * elem == M
+    assert torch.all(block * elem * P * P == M)
+    sent = (block.sum(1) - block.diagonal()) * elem     # bytes each rank sends away
+    assert torch.all(sent * P * P == M * (P - 1))
+
+
 def test_message_sizes_3nh_plus_nh():
-    # Q, K, V exchange 3Nh and the output exchange Nh (hc == hkv, h = hc*hs).
-    sl, bs, hc, hs, P = 64, 1, 8, 16, 4
-    x = torch.zeros(sl, bs, hc, hs)
-    moved = sum(s.numel() for s in oracle.seq_to_head(oracle.shard_sequence(x, P), P))
+    """Q, K and V exchange 3Nh elements and the output Nh (hc == hkv, h = hc*hs), per batch element."""
+    sl, bs, hc, hs, P = 64, 2, 8, 16, 4
     N, h = sl, hc * hs
-    assert 3 * moved == 3 * N * h
-    assert oracle.exchange_bytes(sl, bs, hc, hs, 2) == 2 * N * h * bs
-    # each rank sends (P-1)/P of its shard away: per link M/P
-    per_rank = moved // P
-    assert per_rank == N * h // P
+    x = encoded(sl, bs, hc, hs)
+    moved = sum(s.numel() for s in oracle.seq_to_head(oracle.shard_sequence(x, P), P))
+    assert 3 * moved == 3 * N * h * bs
+    assert 3 * oracle.exchange_bytes(sl, bs, hc, hs, 1) + oracle.exchange_bytes(sl, bs, hc, hs, 1) == 4 * N * h * bs
