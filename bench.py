@@ -23,6 +23,13 @@ same metric through the public API, with the host->device copy of the step's
 inputs and the device->host copy of its outputs inside the timed region.
 ``--impl reference`` times the CPU oracle instead, on a bounded sample.
 
+At N = 1 the line also carries ``configs``: short timed runs, in the same
+process after the headline one, of every other workload (the 128K layer with
+a rows/s figure for the oracle's 1024-row spot check, the packed 64K layer,
+the 8K forward, and the tiny fp32 layer with the whole oracle timed on all
+host cores and on one), each with its kernels' rates and fractions.
+``--no-configs`` skips them.
+
 Under torchrun (N > 1) every rank runs an independent replica of the layer on
 its own GPU. The path has no exchange between GPUs: all P ranks of one layer
 are virtual shards on one GPU. Rank 0 prints the job line.
@@ -214,16 +221,43 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # Our implementation
 # ---------------------------------------------------------------------------
-def run_ours(args, w, rank, world):
+def device_inputs(w, dev):
+    """N(0,1) sequence shards drawn on the device from a generator seeded with the workload's seed.
+
+    For the throughput-only configurations beside the headline workload: the
+    kernels' work depends on the shapes and the mask, not on the values, and
+    a device draw avoids minutes of host-side generation at 128K tokens.
+    """
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    n = w.sl // w.P
+
+    def shards(H):
+        return [torch.randn((n, w.bs, H, w.hs), generator=g, device=dev).to(w.torch_dtype) for _ in range(w.P)]
+
+    out = {"q": shards(w.hc), "k": shards(w.hkv), "v": shards(w.hkv)}
+    if w.backward:
+        out["do"] = shards(w.hc)
+    return out
+
+
+def run_ours(args, w, rank, world, steps=None, warmup=None, with_e2e=None, on_device=False):
+    """Time the layer on workload w; returns the raw timings (run_summary turns them into rates)."""
     import ulysses_sequence_attention_gb300 as U
     from ulysses_sequence_attention_gb300 import _binding as B
 
+    steps = args.steps if steps is None else steps
+    warmup = args.warmup if warmup is None else warmup
+    with_e2e = (not args.no_e2e) if with_e2e is None else with_e2e
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     offs = doc_offsets_for(w)
-    x = make_global_inputs(w)
     P = w.P
-    seq = {k: [t.to(dev) for t in split_shards(v, P)] for k, v in x.items()}
+    if on_device:
+        x = None
+        seq = device_inputs(w, dev)
+    else:
+        x = make_global_inputs(w)
+        seq = {k: [t.to(dev) for t in split_shards(v, P)] for k, v in x.items()}
     fused = None if args.path == "auto" else args.path == "fused"
     L = U.UlyssesLayer(w.sl, w.bs, w.hc, w.hkv, w.hs, P, w.causal, offs, w.torch_dtype, device=str(dev),
                        fused=fused, ds_budget=args.ds_budget)
@@ -298,10 +332,10 @@ def run_ours(args, w, rank, world):
         for i, name in enumerate(U.KERNEL_NAMES):
             ms, n = U.ulysses_timing_read(h, i)
             if n:
-                out[name] = {"total_ms": ms, "launches": n, "ms_per_step": ms / args.steps}
+                out[name] = {"total_ms": ms, "launches": n, "ms_per_step": ms / steps}
         return out
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step(False)
     torch.cuda.synchronize(dev)
     st = U.ulysses_get_status(h)
@@ -317,7 +351,7 @@ def run_ours(args, w, rank, world):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step(True)
     t1.record(stream)
     torch.cuda.synchronize(dev)
@@ -337,7 +371,7 @@ def run_ours(args, w, rank, world):
     torch.cuda.synchronize(dev)
     ev.pop("x0", None), ev.pop("x1", None), ev.pop("x2", None)
     U.ulysses_timing_enable(h, True)
-    for _ in range(args.steps):
+    for _ in range(steps):
         exchange_step()
     torch.cuda.synchronize(dev)
     xk = read_timing()
@@ -355,17 +389,22 @@ def run_ours(args, w, rank, world):
     h2s_ms = statistics.mean(span("x1", "x2"))
 
     elapsed_ms = max_over_ranks(elapsed_ms, dev, world)
-    ms_per_step = elapsed_ms / args.steps
-    value = job_tokens_per_s(w.sl * w.bs, args.steps, world, elapsed_ms)
+    ms_per_step = elapsed_ms / steps
+    value = job_tokens_per_s(w.sl * w.bs, steps, world, elapsed_ms)
 
     e2e = None
-    if not args.no_e2e:
+    if with_e2e and x is not None:
         e2e = run_e2e(args, w, L, x, dev, world, barrier)
 
     result = {"ms_per_step": ms_per_step, "value": value, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
               "s2h_qkv_ms": s2h_ms, "h2s_o_ms": h2s_ms, "launches": launches, "clocks": clk, "e2e": e2e,
               "kernels": kernels, "path": "fused" if L.fused else "explicit",
-              "ds_bytes": B.ulysses_ds_bytes(h)[0] if L.stores_ds else 0}
+              "ds_bytes": B.ulysses_ds_bytes(h)[0] if L.stores_ds else 0, "steps": steps,
+              "timed_s": elapsed_ms / 1e3}
+    del L, seq, hb, ws, lse, o
+    if w.backward:
+        del dq, dk, dv
+    torch.cuda.empty_cache()
     return result
 
 
@@ -469,10 +508,6 @@ def oracle_sample(w, sl_sample):
     return sec, w.sl * w.bs / (sec * work_ratio)
 
 
-def cores_used():
-    return torch.get_num_threads()
-
-
 def run_reference(args, w, rank, world):
     if rank != 0:
         return None
@@ -492,8 +527,8 @@ def run_reference(args, w, rank, world):
             "ms_per_step": 1e3 * statistics.mean(secs), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(w),
-            "cpu_baseline": {"kind": "oracle", "cores": cores_used(), "sample": sample, "value": value,
-                             "unit": "tokens/s"},
+            "cpu_baseline": {"kind": "oracle", "cores": torch.get_num_threads(), **cpu_info(), "sample": sample,
+                             "value": value, "unit": "tokens/s"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return line
@@ -504,6 +539,231 @@ def workload_config(w):
             "hs": w.hs, "causal": w.causal, "ndoc": w.ndoc or 1, "backward": w.backward,
             "parallelism": f"ulysses sp{w.P} (virtual ranks on one GPU)",
             "l2": "inputs larger than L2 (Q alone %.0f MiB)" % (w.sl * w.bs * w.hc * w.hs * w.elem_bytes / 2**20)}
+
+
+# ---------------------------------------------------------------------------
+# Rates, fractions and the roofline of one timed run
+# ---------------------------------------------------------------------------
+FLOP_PER_CYCLE_SM = 8192   # M=256, N=128, K=16 UMMA on a CTA pair every 64 cycles (measured, sm_103a)
+SUSTAINED_AFTER_S = 2.0    # a timed region at least this long is compared with the sustained peak
+
+
+def sm_count():
+    return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+
+
+def run_summary(w, r, peaks, src):
+    """Per-kernel rates and fractions, the attention and exchange figures, and the dominant kernel's roofline.
+
+    Tensor fractions: ``frac_burst`` against the burst cuBLAS bf16 rate,
+    ``frac_sustained`` against the rate cuBLAS holds for seconds under the
+    power cap, and ``frac_of_clock_peak`` against the UMMA issue rate at the
+    SM clock sampled during the run (8192 flop/cycle/SM x SMs x median MHz).
+    ``frac`` is the burst fraction for a timed region under two seconds, the
+    sustained one otherwise.
+    """
+    steps = r["steps"]
+    offs = doc_offsets_for(w)
+    burst = peaks["bf16_tflops"]
+    sustained = peaks.get("bf16_tflops_sustained", burst)
+    long_run = r["timed_s"] >= SUSTAINED_AFTER_S
+    clk = (r["clocks"] or {}).get("sm_mhz")
+    clock_peak = FLOP_PER_CYCLE_SM * sm_count() * clk * 1e6 / 1e12 if clk else None
+
+    def tensor_fracs(tf):
+        if w.dtype != "bf16":   # the fp32 path runs on the CUDA cores: no bf16 tensor peak applies
+            return {"tflops": tf}
+        out = {"tflops": tf, "frac_burst": tf / burst, "frac_sustained": tf / sustained}
+        if clock_peak:
+            out["frac_of_clock_peak"] = tf / clock_peak
+        return out
+
+    fl_fwd = attn_flops(w, offs=offs)
+    fl_bwd = 2.5 * fl_fwd if w.backward else 0.0
+    ds_blocks = max(r["ds_bytes"] - 32768, 0)   # the stored blocks, zero block excluded
+    work = kernel_work(w, offs, ds_blocks)
+    per_kernel = {}
+    for name, k in r["kernels"].items():
+        cname, bound, units, unit = work[name]
+        rate = units * steps / (k["total_ms"] * 1e-3)
+        per_kernel[name] = dict(k, kernel=cname, bound=bound,
+                                **(tensor_fracs(rate / 1e12) if unit == "flop" else
+                                   {"gbs": rate / 1e9, "frac_hbm": rate / 1e9 / peaks["hbm_gbs"]}))
+        if name == "bwd_dq" and not ds_blocks:   # S and dP are issued again here: 3 GEMMs run, 1 is its own
+            per_kernel[name]["issued_tflops"] = 3 * rate / 1e12
+    km = {n: k["ms_per_step"] for n, k in r["kernels"].items()}
+    attn_fwd_ms = km["attn_fwd"]
+    attn_bwd_ms = sum(km.get(n, 0.0) for n in ("bwd_prep", "bwd_dkdv", "bwd_dq"))
+    fwd_tf = fl_fwd / (attn_fwd_ms * 1e-3) / 1e12
+    bwd_tf = fl_bwd / (attn_bwd_ms * 1e-3) / 1e12 if w.backward else None
+    x_bytes = exchange_bytes(w, w.hc) + 2 * exchange_bytes(w, w.hkv)
+    s2h_gbs = x_bytes / (r["s2h_qkv_ms"] * 1e-3) / 1e9
+    h2s_gbs = exchange_bytes(w, w.hc) / (r["h2s_o_ms"] * 1e-3) / 1e9
+    # the dominant kernel: the largest share of the timed step's device time
+    top = max((n for n in r["kernels"] if "region" not in r["kernels"][n]),
+              key=lambda n: r["kernels"][n]["total_ms"])
+    cname, bound, units, unit = work[top]
+    k = r["kernels"][top]
+    avg_ms = k["total_ms"] / k["launches"]
+    per_launch = units * steps / k["launches"]
+    achieved = per_launch / (avg_ms * 1e-3) / (1e12 if unit == "flop" else 1e9)
+    if unit == "flop":
+        peak, peak_name = (sustained, "bf16_tflops_sustained") if long_run else (burst, "bf16_tflops")
+    else:
+        peak, peak_name = peaks["hbm_gbs"], "hbm_gbs"
+    traffic, traffic_how = captured_traffic(cname, w.name)
+    roof = {"bound": bound, "kernel": cname, "achieved": achieved, "peak": peak,
+            "unit": "TFLOP/s" if unit == "flop" else "GB/s", "frac": achieved / peak, "traffic": traffic,
+            "traffic_source": traffic_how,
+            "peak_source": f"{src} {peak_name} (timed region {r['timed_s']:.2f} s: "
+                           f"{'sustained' if long_run else 'burst'} peak)",
+            "algorithmic_per_launch": per_launch, "algorithmic_unit": unit, "avg_launch_ms": avg_ms,
+            "launches": k["launches"],
+            "share_of_step": k["total_ms"] / (r["ms_per_step"] * steps),
+            "timing": "CUDA events recorded by the library around each launch on its stream"}
+    if unit == "flop":
+        roof.update({"frac_sustained": achieved / sustained, "frac_burst": achieved / burst})
+        if clock_peak:
+            roof["frac_of_clock_peak"] = achieved / clock_peak
+            roof["clock_peak"] = {"tflops": clock_peak, "sm_mhz": clk, "sms": sm_count(),
+                                  "flop_per_cycle_sm": FLOP_PER_CYCLE_SM}
+    attention = {"fwd_ms": attn_fwd_ms, "fwd_tflop": fl_fwd / 1e12,
+                 **{"fwd_" + a: b for a, b in tensor_fracs(fwd_tf).items()},
+                 "kernel_times": "per-kernel CUDA events: forward kernel; backward prep + dK/dV + dQ",
+                 "layer_fwd_ms": r["fwd_ms"],
+                 "layer_times": "CUDA events around the layer's forward and backward calls (exchanges included)"}
+    if w.backward:
+        attention.update({"bwd_ms": attn_bwd_ms, "bwd_tflop": fl_bwd / 1e12,
+                          **{"bwd_" + a: b for a, b in tensor_fracs(bwd_tf).items()},
+                          # 4 GEMMs (2.0x the forward): the figure without recomputing S
+                          "bwd_tflops_no_recompute": 0.8 * bwd_tf, "layer_bwd_ms": r["bwd_ms"]})
+    exchange = {"s2h_qkv_ms": r["s2h_qkv_ms"], "s2h_qkv_gbs": s2h_gbs, "s2h_qkv_frac_hbm": s2h_gbs / peaks["hbm_gbs"],
+                "h2s_o_ms": r["h2s_o_ms"], "h2s_o_gbs": h2s_gbs, "h2s_o_frac_hbm": h2s_gbs / peaks["hbm_gbs"],
+                "bytes_rule": "read + write of the whole tensor per exchange",
+                "timed": ("the explicit exchange kernels in a loop of their own; the fused step runs none "
+                          "(the attention kernels read and write the sequence shards)" if r["path"] == "fused" else
+                          "the explicit exchange kernels, in a loop of their own"),
+                "hbm_peak_gbs": peaks["hbm_gbs"], "hbm_peak_source": src}
+    backward_dq = None
+    if w.backward:
+        backward_dq = ({"how": "stored dS: the dK/dV kernel writes bf16 dS, dQ = s dS K reads it back",
+                        "ds_bytes": r["ds_bytes"]} if ds_blocks else
+                       {"how": "recomputed: the dQ kernel forms S, P, dP and dS again"})
+    return {"kernels": per_kernel, "roofline": roof, "attention": attention, "exchange": exchange,
+            "backward_dq": backward_dq}
+
+
+# The other workloads of the layer, timed in the same process after the
+# headline one: (workload, timed steps, inputs drawn on the device).
+OTHER_CONFIGS = (("alst_128k", 4, True), ("packed_64k", 10, True), ("llama8b_8k", 20, True), ("tiny", 20, False))
+
+
+def run_configs(args, main_w, rank, world):
+    """Short timed runs of every other workload (N = 1), each summarised like the headline one."""
+    peaks, src = load_peaks()
+    out = {}
+    for name, steps, on_device in OTHER_CONFIGS:
+        if name == main_w.name:
+            continue
+        w = WORKLOADS[name]
+        r = run_ours(args, w, rank, world, steps=steps, warmup=3, with_e2e=False, on_device=on_device)
+        rs = run_summary(w, r, peaks, src)
+        entry = {"config": workload_config(w), "steps": steps, "ms_per_step": r["ms_per_step"],
+                 "tokens_per_s": r["value"], "path": r["path"], "clocks": r["clocks"],
+                 "inputs": ("device-side N(0,1) draw of the workload's shapes, seeded with its seed"
+                            if on_device else "the workload's seeded host recipe"),
+                 "kernels": {n: {a: b for a, b in k.items() if a not in ("total_ms", "launches")}
+                             for n, k in rs["kernels"].items()},
+                 "attention": rs["attention"], "exchange": {a: b for a, b in rs["exchange"].items()
+                                                            if a.endswith(("_ms", "_gbs", "_hbm"))},
+                 "roofline": {a: rs["roofline"][a] for a in ("kernel", "bound", "achieved", "unit", "frac",
+                                                              "frac_burst", "frac_sustained", "frac_of_clock_peak")
+                              if a in rs["roofline"]},
+                 "backward_dq": rs["backward_dq"]}
+        if name == "tiny":
+            entry["oracle"] = oracle_whole_layer_timing(w)
+        if name == "alst_128k":
+            entry["oracle_spot_check"] = oracle_row_sample_timing(w, 1024)
+        out[name] = entry
+    return out
+
+
+def cpu_info():
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    model = None
+    try:
+        p = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in p.stdout.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                model = line.split(":", 1)[1].strip()
+                if line.startswith("Model name"):
+                    break
+    except Exception:
+        pass
+    import platform
+    return {"cores_available": cores, "cpu_model": model or platform.processor() or platform.machine()}
+
+
+def with_threads(n, fn):
+    old = torch.get_num_threads()
+    torch.set_num_threads(n)
+    try:
+        return fn()
+    finally:
+        torch.set_num_threads(old)
+
+
+def cpu_baseline(w, sl_sample):
+    info = cpu_info()
+    n = info["cores_available"]
+    sec, val = with_threads(n, lambda: oracle_sample(w, sl_sample))
+    return {"value": val, "unit": "tokens/s", "cores": n, "kind": "oracle", **info,
+            "sample": (f"oracle (torch fp64 CPU, {n} threads) whole layer {'fwd+bwd' if w.backward else 'fwd'} "
+                       f"at sl={sl_sample} (same P/heads/hs/mask) took {sec:.2f} s; tokens/s scaled to "
+                       f"sl={w.sl} by visible-pair work")}
+
+
+def oracle_whole_layer_timing(w):
+    """The oracle on the whole (small) workload: all host cores, then one."""
+    info = cpu_info()
+    res = {**info}
+    oracle_sample(w, w.sl)   # untimed first call (library set-up, page-ins)
+    for label, n in (("all_cores", info["cores_available"]), ("one_core", 1)):
+        sec, _ = with_threads(n, lambda: oracle_sample(w, w.sl))
+        res[label] = {"threads": n, "seconds": sec, "tokens_per_s": w.sl * w.bs / sec}
+    return res
+
+
+def oracle_row_sample_timing(w, rows):
+    """The oracle's spot check of the 128K workload: O, LSE and dQ of `rows` random query rows.
+
+    Rows/s of the sampled check, and the extrapolation to every row of the
+    layer (labelled as such: the full oracle at this size is ~490 TFLOP of fp64).
+    """
+    import oracle
+    import numpy as np
+    info = cpu_info()
+    g = torch.Generator("cpu").manual_seed(w.seed)
+    rng = np.random.default_rng(w.seed)
+    heads = 32
+    per_head = rows // heads
+    s = 1.0 / math.sqrt(w.hs)
+    # one head's tensors serve every head: the check's cost depends on the shapes only
+    q, k, v, do = (torch.randn(w.sl, w.hs, generator=g, dtype=torch.float64) for _ in range(4))
+
+    def run():
+        t0 = time.perf_counter()
+        for _ in range(heads):
+            rr = torch.tensor(np.sort(rng.choice(w.sl, per_head, replace=False)))
+            oracle.attention_head_dq_rows(q, k, v, do, s, w.causal, doc_offsets_for(w), rr)
+        return time.perf_counter() - t0
+
+    sec = with_threads(info["cores_available"], run)
+    n = heads * per_head
+    total_rows = w.sl * w.bs * w.hc
+    return {**info, "threads": info["cores_available"], "rows": n, "seconds": sec, "rows_per_s": n / sec,
+            "extrapolated_layer_fwd_s": total_rows / (n / sec),
+            "note": "rows/s of the sampled O/LSE/dQ check; the layer figure is an extrapolation, not a run"}
 
 
 # ---------------------------------------------------------------------------
@@ -521,6 +781,8 @@ def main():
     ap.add_argument("--ds-budget", type=int, default=None,
                     help="bytes the backward may keep dS in (default: the layer's; 0 recomputes dQ)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the short timed runs of the other workloads (the `configs` object)")
     ap.add_argument("--cpu-sl", type=int, default=4096, help="oracle sample length for cpu_baseline")
     ap.add_argument("--ref-sl", type=int, default=1024, help="oracle sample length per reference step")
     ap.add_argument("--sl", type=int, default=None,
@@ -549,94 +811,32 @@ def main():
         torch.distributed.init_process_group("nccl")
 
     r = run_ours(args, w, rank, world)
+    configs = None
+    if not args.no_configs and world == 1:
+        configs = run_configs(args, w, rank, world)
     if rank == 0:
         peaks, src = load_peaks()
-        offs = doc_offsets_for(w)
-        fl_fwd = attn_flops(w, offs=offs)
-        fl_bwd = 2.5 * fl_fwd if w.backward else 0.0
-        km = {n: k["ms_per_step"] for n, k in r["kernels"].items()}
-        attn_fwd_ms = km["attn_fwd"]
-        attn_bwd_ms = sum(km.get(n, 0.0) for n in ("bwd_prep", "bwd_dkdv", "bwd_dq"))
-        fwd_tf = fl_fwd / (attn_fwd_ms * 1e-3) / 1e12
-        bwd_tf = fl_bwd / (attn_bwd_ms * 1e-3) / 1e12 if w.backward else None
-        x_bytes = exchange_bytes(w, w.hc) + 2 * exchange_bytes(w, w.hkv)
-        s2h_gbs = x_bytes / (r["s2h_qkv_ms"] * 1e-3) / 1e9
-        h2s_gbs = exchange_bytes(w, w.hc) / (r["h2s_o_ms"] * 1e-3) / 1e9
-        sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-        ds_blocks = max(r["ds_bytes"] - 32768, 0)   # the stored blocks, zero block excluded
-        work = kernel_work(w, offs, ds_blocks)
-        per_kernel = {}
-        for name, k in r["kernels"].items():
-            cname, bound, units, unit = work[name]
-            rate = units * args.steps / (k["total_ms"] * 1e-3)
-            per_kernel[name] = dict(k, kernel=cname, bound=bound,
-                                    **({"tflops": rate / 1e12, "frac_sustained": rate / 1e12 / sustained}
-                                       if unit == "flop" else
-                                       {"gbs": rate / 1e9, "frac_hbm": rate / 1e9 / peaks["hbm_gbs"]}))
-            if name == "bwd_dq" and not ds_blocks:   # S and dP are issued again here: 3 GEMMs run, 1 is its own
-                per_kernel[name]["issued_tflops"] = 3 * rate / 1e12
-        # the dominant kernel: the largest share of the timed step's device time
-        top = max((n for n in r["kernels"] if "region" not in r["kernels"][n]),
-                  key=lambda n: r["kernels"][n]["total_ms"])
-        cname, bound, units, unit = work[top]
-        k = r["kernels"][top]
-        avg_ms = k["total_ms"] / k["launches"]
-        per_launch = units * args.steps / k["launches"]
-        achieved = per_launch / (avg_ms * 1e-3) / (1e12 if unit == "flop" else 1e9)
-        peak = sustained if unit == "flop" else peaks["hbm_gbs"]
-        traffic, traffic_how = captured_traffic(cname, w.name)
-        roof = {"bound": bound, "kernel": cname, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s" if unit == "flop" else "GB/s", "frac": achieved / peak, "traffic": traffic,
-                "traffic_source": traffic_how,
-                "peak_source": f"{src} " + ("bf16_tflops_sustained" if unit == "flop" else "hbm_gbs"),
-                "algorithmic_per_launch": per_launch, "algorithmic_unit": unit, "avg_launch_ms": avg_ms,
-                "launches": k["launches"],
-                "share_of_step": k["total_ms"] / (r["ms_per_step"] * args.steps),
-                "timing": "CUDA events recorded by the library around each launch on its stream"}
-        if unit == "flop":
-            roof["frac_of_burst"] = achieved / peaks["bf16_tflops"]
+        rs = run_summary(w, r, peaks, src)
         cpu = None
         if not args.no_cpu_baseline:
-            sec, val = oracle_sample(w, args.cpu_sl)
-            cpu = {"value": val, "unit": "tokens/s", "cores": cores_used(), "kind": "oracle",
-                   "sample": (f"oracle (torch fp64 CPU) whole layer {'fwd+bwd' if w.backward else 'fwd'} at "
-                              f"sl={args.cpu_sl} (same P/heads/hs/mask) took {sec:.2f} s; tokens/s scaled to "
-                              f"sl={w.sl} by visible-pair work")}
+            cpu = cpu_baseline(w, args.cpu_sl)
         line = {"metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16" if w.dtype == "bf16" else "f32",
                 "data": "synthetic (seeded N(0,1) Q/K/V/dO of the workload's shape)",
                 "config": workload_config(w),
-                "roofline": roof,
+                "roofline": rs["roofline"],
                 "cpu_baseline": cpu,
                 "e2e": r["e2e"],
                 "gpu_launches": r["launches"],
-                "kernels": per_kernel,
+                "kernels": rs["kernels"],
                 "clocks": r["clocks"],
                 "path": r["path"],
-                "backward_dq": ({"how": "stored dS: the dK/dV kernel writes bf16 dS, dQ = s dS K reads it back",
-                                 "ds_bytes": r["ds_bytes"]} if ds_blocks else
-                                {"how": "recomputed: the dQ kernel forms S, P, dP and dS again"}),
-                "attention": {"fwd_ms": attn_fwd_ms, "fwd_tflops": fwd_tf, "fwd_frac_sustained": fwd_tf / sustained,
-                              "bwd_ms": attn_bwd_ms, "bwd_tflops": bwd_tf,
-                              # 4 GEMMs (2.0x the forward): the figure without recomputing S
-                              "bwd_tflops_no_recompute": (0.8 * bwd_tf) if bwd_tf else None,
-                              "bwd_frac_sustained": (bwd_tf / sustained) if bwd_tf else None,
-                              "fwd_tflop": fl_fwd / 1e12, "bwd_tflop": fl_bwd / 1e12,
-                              "kernel_times": "per-kernel CUDA events: forward kernel; backward prep + dK/dV + dQ",
-                              "layer_fwd_ms": r["fwd_ms"], "layer_bwd_ms": r["bwd_ms"],
-                              "layer_times": "CUDA events around the layer's forward and backward calls "
-                                             "(exchanges included)"},
-                "exchange": {"s2h_qkv_ms": r["s2h_qkv_ms"], "s2h_qkv_gbs": s2h_gbs,
-                             "s2h_qkv_frac_hbm": s2h_gbs / peaks["hbm_gbs"],
-                             "h2s_o_ms": r["h2s_o_ms"], "h2s_o_gbs": h2s_gbs,
-                             "h2s_o_frac_hbm": h2s_gbs / peaks["hbm_gbs"],
-                             "bytes_rule": "read + write of the whole tensor per exchange",
-                             "timed": ("the explicit exchange kernels in a loop of their own; the fused step runs "
-                                       "none (the attention kernels read and write the sequence shards)"
-                                       if r["path"] == "fused" else "the explicit exchange kernels, in a loop of "
-                                       "their own"),
-                             "hbm_peak_gbs": peaks["hbm_gbs"], "hbm_peak_source": src},
+                "backward_dq": rs["backward_dq"],
+                "attention": rs["attention"],
+                "exchange": rs["exchange"],
+                "configs": configs,
                 "context": "pages' figure (not a target): ALST trains a 500K-token sequence for Llama-8B on one H100"}
         print(json.dumps(line), flush=True)
     if world > 1:
