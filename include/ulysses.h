@@ -33,7 +33,7 @@
  *    it alive until the work queued on the stream has finished.
  *  - Streams. `stream` is a cudaStream_t (NULL = legacy default stream). Every
  *    device call only enqueues work on it and returns without synchronising.
- *    The one exception is ulysses_get_status.
+ *    The one exception is ulysses_get_status, which waits for one stream.
  *  - Errors. Every int-returning call returns ULYSSES_OK (0) or a negative
  *    ulysses_status. No C++ exception crosses this boundary. Arguments are
  *    checked before anything is enqueued. A failed check enqueues nothing.
@@ -416,10 +416,12 @@ int ulysses_host_end(ulysses_t h, void* stream);
 
 /*
  * ulysses_get_status — read and clear the handle's device status word.
- * Synchronises the device. Returns ULYSSES_OK, ULYSSES_ERR_TIMEOUT if a
- * bounded device-side wait ran out since the last call (the kernel then
- * returned early and its outputs are invalid), or ULYSSES_ERR_CUDA if the
- * device reports an error.
+ * The read and the clear are enqueued on the stream of the handle's latest
+ * call that took a stream, and this call waits for that stream only: work of
+ * the handle enqueued on other streams must be ordered before it by the
+ * caller. Returns ULYSSES_OK, ULYSSES_ERR_TIMEOUT if a bounded device-side
+ * wait ran out since the last call (the kernel then returned early and its
+ * outputs are invalid), or ULYSSES_ERR_CUDA if the stream reports an error.
  */
 int ulysses_get_status(ulysses_t h);
 

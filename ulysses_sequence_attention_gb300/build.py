@@ -3,14 +3,23 @@
 Each ``csrc/*.cu`` is compiled in parallel into ``_build/`` and linked into
 ``libulysses.so`` next to this file. The CUDA runtime is linked statically,
 and the driver API is reached through ``cudaGetDriverEntryPointByVersion``, so
-the library loads on a host without a GPU driver. A rebuild happens only when
-a source or header is newer than the library.
+the library loads on a host without a GPU driver.
+
+What is rebuilt follows content, not file times: each object records a key
+(sha256 over its source, every header, the compiler flags, the compiler's
+version and the host's machine type) in ``_build/<name>.key``, and the
+library records the keys of the objects it was linked from. An object or a
+library whose key differs from the current one, or is missing, is built
+again, so a stale or foreign binary copied in beside the sources is never
+reused.
 """
 from __future__ import annotations
 
 import concurrent.futures
 import glob
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -41,27 +50,53 @@ def _headers():
     return sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
-def _newest(paths):
-    return max((os.path.getmtime(p) for p in paths), default=0.0)
+def _compiler_id(nvcc: str) -> str:
+    p = subprocess.run([nvcc, "--version"], capture_output=True, text=True)
+    return p.stdout.strip().splitlines()[-1] if p.returncode == 0 and p.stdout.strip() else nvcc
+
+
+def _key(parts) -> str:
+    h = hashlib.sha256()
+    for part in parts:
+        h.update(part if isinstance(part, bytes) else str(part).encode())
+        h.update(b"\0")
+    return h.hexdigest()
+
+
+def _read(path: str) -> str:
+    try:
+        with open(path) as f:
+            return f.read().strip()
+    except OSError:
+        return ""
 
 
 def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
     """Compile every kernel source and link the shared library. Returns its path."""
     srcs = _sources()
-    hdr_time = _newest(_headers())
     os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = _nvcc()
-    jobs = []
+    common = [_compiler_id(nvcc), platform.machine(), " ".join(NVCC_FLAGS)]
+    common += [open(h, "rb").read() for h in _headers()]
+    jobs, keys = [], {}
     for src in srcs:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-        if force or not os.path.exists(obj) or os.path.getmtime(obj) < max(os.path.getmtime(src), hdr_time):
+        base = os.path.basename(src)[:-3]
+        obj = os.path.join(BUILD_DIR, base + ".o")
+        keys[src] = _key(common + [base, open(src, "rb").read(), ptxas_verbose])
+        if force or not os.path.exists(obj) or _read(os.path.join(BUILD_DIR, base + ".key")) != keys[src]:
             cmd = [nvcc] + NVCC_FLAGS + (["-Xptxas", "-v"] if ptxas_verbose else []) + ["-c", src, "-o", obj]
             jobs.append((src, cmd))
     objs = [os.path.join(BUILD_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
 
     def run(job):
         src, cmd = job
+        keyfile = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".key")
+        if os.path.exists(keyfile):
+            os.unlink(keyfile)      # no key for an object while it is being rewritten
         p = subprocess.run(cmd, capture_output=True, text=True)
+        if p.returncode == 0:
+            with open(keyfile, "w") as f:
+                f.write(keys[src])
         return src, p.returncode, p.stdout + p.stderr
 
     if jobs:
@@ -71,13 +106,17 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
                     sys.stderr.write(f"== {os.path.basename(src)}\n{out}")
                 if rc != 0:
                     raise RuntimeError(f"nvcc failed on {src}")
-    if force or jobs or not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < _newest(objs):
+    lib_key = _key([keys[s] for s in srcs] + [" ".join(ARCH)])
+    lib_keyfile = os.path.join(BUILD_DIR, "libulysses.key")
+    if force or jobs or not os.path.exists(LIB_PATH) or _read(lib_keyfile) != lib_key:
         tmp = LIB_PATH + ".tmp"
         cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
         p = subprocess.run(cmd, capture_output=True, text=True)
         if p.returncode != 0:
             raise RuntimeError("link failed:\n" + p.stdout + p.stderr)
         os.replace(tmp, LIB_PATH)
+        with open(lib_keyfile, "w") as f:
+            f.write(lib_key)
     return LIB_PATH
 
 

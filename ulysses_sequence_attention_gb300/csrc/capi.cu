@@ -225,6 +225,7 @@ int ulysses_create_varlen(ulysses_t* out, int64_t max_sl, int64_t bs, int hc, in
 int ulysses_set_seq(ulysses_t h, int64_t sl, const int32_t* doc_offsets, int ndoc, void* stream) {
   Layer* L = reinterpret_cast<Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
+  L->last_stream = (cudaStream_t)stream;
   if (sl > L->cap_sl) return ULYSSES_ERR_TOO_LARGE;
   int st = check_seq(sl, L->cap_sl, L->P, doc_offsets, ndoc, L->cap_docs);
   if (st != ULYSSES_OK) return st;
@@ -270,6 +271,7 @@ int ulysses_seq_to_head(ulysses_t h, int nheads, const void* const* seq_shards,
                         void* const* head_shards, void* stream) {
   const Layer* L = reinterpret_cast<const Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
+  L->last_stream = (cudaStream_t)stream;
   if (nheads != L->hc && nheads != L->hkv) return ULYSSES_ERR_INVALID_ARG;
   if (L->empty()) return ULYSSES_OK;
   CHECK_PTRS(seq_shards);
@@ -281,6 +283,7 @@ int ulysses_head_to_seq(ulysses_t h, int nheads, const void* const* head_shards,
                         void* const* seq_shards, void* stream) {
   const Layer* L = reinterpret_cast<const Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
+  L->last_stream = (cudaStream_t)stream;
   if (nheads != L->hc && nheads != L->hkv) return ULYSSES_ERR_INVALID_ARG;
   if (L->empty()) return ULYSSES_OK;
   CHECK_PTRS(head_shards);
@@ -293,6 +296,7 @@ int ulysses_seq_to_head_qkv(ulysses_t h, const void* const* q_seq, const void* c
                             void* stream) {
   const Layer* L = reinterpret_cast<const Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
+  L->last_stream = (cudaStream_t)stream;
   if (L->empty()) return ULYSSES_OK;
   CHECK_PTRS(q_seq);
   CHECK_PTRS(k_seq);
@@ -311,6 +315,7 @@ int ulysses_head_to_seq_qkv(ulysses_t h, const void* const* q_head, const void* 
                             void* stream) {
   const Layer* L = reinterpret_cast<const Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
+  L->last_stream = (cudaStream_t)stream;
   if (L->empty()) return ULYSSES_OK;
   CHECK_PTRS(q_head);
   CHECK_PTRS(k_head);
@@ -328,6 +333,7 @@ int ulysses_attn_fwd(ulysses_t h, const void* const* q, const void* const* k,
                      const void* const* v, void* const* o, float* const* lse, void* stream) {
   Layer* L = reinterpret_cast<Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
+  L->last_stream = (cudaStream_t)stream;
   if (L->empty()) return ULYSSES_OK;
   CHECK_PTRS(q);
   CHECK_PTRS(k);
@@ -389,6 +395,7 @@ int attn_bwd_entry(ulysses_t h, const void* const* q, const void* const* k, cons
                    void* const* dk, void* const* dv, void* workspace, void* stream, bool store_ds) {
   const Layer* L = reinterpret_cast<const Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
+  L->last_stream = (cudaStream_t)stream;
   if (L->empty()) return ULYSSES_OK;
   CHECK_PTRS(q);
   CHECK_PTRS(k);
@@ -421,6 +428,7 @@ int ulysses_layer_fwd(ulysses_t h, const void* const* q, const void* const* k, c
                       void* const* o, float* const* lse, void* stream) {
   Layer* L = reinterpret_cast<Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
+  L->last_stream = (cudaStream_t)stream;
   if (L->empty()) return ULYSSES_OK;
   if (!uly::fused_supported(*L)) return ULYSSES_ERR_UNSUPPORTED;
   CHECK_PTRS(q);
@@ -436,6 +444,7 @@ int ulysses_layer_bwd(ulysses_t h, const void* const* q, const void* const* k, c
                       void* const* dk, void* const* dv, void* workspace, void* stream) {
   const Layer* L = reinterpret_cast<const Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
+  L->last_stream = (cudaStream_t)stream;
   if (L->empty()) return ULYSSES_OK;
   if (!uly::fused_supported(*L)) return ULYSSES_ERR_UNSUPPORTED;
   CHECK_PTRS(q);
@@ -489,11 +498,15 @@ int ulysses_timing_read(ulysses_t h, int kernel, double* total_ms, int64_t* laun
 int ulysses_get_status(ulysses_t h) {
   const Layer* L = reinterpret_cast<const Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
-  if (cudaDeviceSynchronize() != cudaSuccess) return ULYSSES_ERR_CUDA;
+  // In order on the stream of the handle's latest call: the read follows that
+  // stream's work, the clear precedes anything enqueued on it later, and only
+  // that stream is waited for.
+  const cudaStream_t s = L->last_stream;
   unsigned word = 0;
-  if (cudaMemcpy(&word, L->d_status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpyAsync(&word, L->d_status, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return ULYSSES_ERR_CUDA;
-  if (cudaMemset(L->d_status, 0, sizeof(unsigned)) != cudaSuccess) return ULYSSES_ERR_CUDA;
+  if (cudaMemsetAsync(L->d_status, 0, sizeof(unsigned), s) != cudaSuccess) return ULYSSES_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return ULYSSES_ERR_CUDA;
   if (word & uly::STATUS_TIMEOUT) return ULYSSES_ERR_TIMEOUT;
   return ULYSSES_OK;
 }

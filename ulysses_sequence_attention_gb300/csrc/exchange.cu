@@ -10,7 +10,7 @@
 // Hh*hs elements in both layouts. The kernels move whole 16-byte vectors.
 // Every thread keeps UNROLL independent loads in flight before it stores, so
 // an SM holds enough bytes in flight to saturate HBM. The grid is a whole
-// number of waves over the 152 SMs. Index arithmetic uses multiply-shift
+// number of waves over the device's SMs. Index arithmetic uses multiply-shift
 // division by invariant integers (Granlund and Montgomery, "Division by
 // invariant integers using multiplication", PLDI 1994).
 #include "internal.cuh"
@@ -38,7 +38,6 @@ struct FastDiv {
 
 constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
-constexpr int kSMs = 152;
 
 struct S2HArgs {
   RankPtrs src;        // P sequence shards [n][bs][H][hs]
@@ -208,7 +207,7 @@ __global__ void __launch_bounds__(kThreads) head_to_seq_sum_kernel(RankPtrs src,
 
 int grid_for(uint64_t items_per_thread_block) {
   uint64_t g = (items_per_thread_block + (uint64_t)kThreads * kUnroll - 1) / ((uint64_t)kThreads * kUnroll);
-  const uint64_t cap = (uint64_t)kSMs * 8;  // 8 resident 256-thread blocks per SM
+  const uint64_t cap = (uint64_t)device_sm_count() * 8;  // 8 resident 256-thread blocks per SM
   if (g > cap) g = cap;
   if (g < 1) g = 1;
   return (int)g;
@@ -316,7 +315,7 @@ int launch_head_to_seq(const Layer& L, int nheads, const void* const* src, void*
       d.p[r] = dst[r];
     }
     uint64_t g = (total + kThreads - 1) / kThreads;
-    if (g > (uint64_t)kSMs * 8) g = (uint64_t)kSMs * 8;
+    if (g > (uint64_t)device_sm_count() * 8) g = (uint64_t)device_sm_count() * 8;
     Timed t(L.timing, ULYSSES_KERNEL_HEAD_TO_SEQ, stream);
     if (L.dtype == ULYSSES_BF16)
       head_to_seq_sum_kernel<__nv_bfloat16><<<(int)g, kThreads, 0, stream>>>(

@@ -78,6 +78,7 @@ extern "C" {
 int ulysses_host_begin(ulysses_t h, void* stream) {
   Layer* L = reinterpret_cast<Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
+  L->last_stream = (cudaStream_t)stream;
   if (!uly::fused_supported(*L) && !L->empty()) return ULYSSES_ERR_UNSUPPORTED;
   int st = uly::ensure_pipe(*L);
   if (st != ULYSSES_OK) return st;
@@ -92,6 +93,7 @@ int ulysses_host_step(ulysses_t h, int slot, const void* const* host_in, void* c
                       float* const* lse, void* workspace, void* stream) {
   Layer* L = reinterpret_cast<Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
+  L->last_stream = (cudaStream_t)stream;
   if (slot != 0 && slot != 1) return ULYSSES_ERR_INVALID_ARG;
   if (L->empty()) return ULYSSES_OK;
   if (!uly::fused_supported(*L)) return ULYSSES_ERR_UNSUPPORTED;
@@ -169,6 +171,7 @@ int ulysses_host_step(ulysses_t h, int slot, const void* const* host_in, void* c
 int ulysses_host_end(ulysses_t h, void* stream) {
   Layer* L = reinterpret_cast<Layer*>(h);
   if (!L) return ULYSSES_ERR_INVALID_ARG;
+  L->last_stream = (cudaStream_t)stream;
   if (!L->pipe.ready) return ULYSSES_OK;  // no step was ever enqueued
   Layer::HostPipe& p = L->pipe;
   cudaError_t e = cudaEventRecord(p.h2d_tail, p.h2d);

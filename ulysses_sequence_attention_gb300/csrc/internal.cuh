@@ -125,6 +125,9 @@ struct Layer {
   std::vector<int32_t> doc_offsets;   // host copy, ndoc + 1 entries
   int32_t* d_doc_offsets = nullptr;   // device copy, ndoc + 1 entries
   unsigned* d_status = nullptr;       // device status word
+  // The stream of the handle's latest enqueuing call: ulysses_get_status
+  // reads the status word in order on it (set by every call that takes a stream).
+  mutable cudaStream_t last_stream = nullptr;
   int device = 0;
   // Tensor-core path (CTA pairs): per 256-key pair tile the range of 128-row
   // query tiles that see it (dK/dV), per 256-query pair tile the range of
@@ -270,6 +273,25 @@ int64_t ds_blocks_at_capacity(const Layer& L);
 int attn_bwd_entry(ulysses_t h, const void* const* q, const void* const* k, const void* const* v,
                    const void* const* o, const void* const* dO, const float* const* lse, void* const* dq,
                    void* const* dk, void* const* dv, void* workspace, void* stream, bool store_ds);
+
+// Number of SMs of the current device, looked up once per device (grid
+// sizing of the streaming kernels).
+inline int device_sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64) {
+    const int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 1;
+  }
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
 
 // Looks up, and so loads, the no-alloc scratch array on the current device
 // (noalloc.cu); ulysses_create calls it during set-up.
