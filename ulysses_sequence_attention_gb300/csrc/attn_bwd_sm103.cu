@@ -496,23 +496,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + lane_base + 128 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
       tmem_ld32(tmem + lane_base + 160 + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
       tmem_ld_wait(dp);
+      // P^T and dS^T (bf16) over the dP^T columns this thread has just read
+      // (no other thread reads them); the store of P^T runs while dS^T is
+      // formed.
+      tmem_st32(tmem + lane_base + 128 + 64 * h, pk);
       // dS^T = P^T * (dP^T - D)
       const uint64_t* d2 = reinterpret_cast<const uint64_t*>(rs + 128 + 64 * h);
       uint32_t dk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) dk[c] = f2_pack_bf16(f2_mul(pp[c], f2_sub(f2_bits(dp[2 * c], dp[2 * c + 1]), d2[c])));
+      tmem_st32(tmem + lane_base + 160 + 64 * h, dk);
+      tmem_st_wait(pk);
+      tc_fence_before();
+      warp_arrive_leader(bar(B_P), crank);
       // Done with this tile's LSE/D rows. The producer refills the slot by
       // TMA (the async proxy) once every warp has arrived: the proxy fence
       // orders this thread's generic reads of the slot before that write.
       fence_proxy_async_smem();
       warp_arrive_local(bar(B_REMPTY + rsl));
-      // P^T and dS^T (bf16) over the dP^T columns this thread has just read:
-      // no other thread reads them
-      tmem_st32(tmem + lane_base + 128 + 64 * h, pk);
-      tmem_st32(tmem + lane_base + 160 + 64 * h, dk);
-      tmem_st_wait();
-      tc_fence_before();
-      warp_arrive_leader(bar(B_P), crank);
       if (kStore) {
         // dS^T row jr = column jr of dS, staged for the store thread once it
         // has read the previous tile's image out.

@@ -197,6 +197,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// The same wait for a store whose source registers stay in use past other
+// work: each register is read by an empty volatile asm after the wait, so
+// the compiler keeps it (and does not reuse it) until the store is complete.
+template <int N>
+__device__ __forceinline__ void tmem_st_wait(const uint32_t (&r)[N]) {
+  tmem_st_wait();
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" ::"r"(r[i]));
+}
 
 // Per-warpgroup register budget changes. All four warps of a warpgroup
 // execute them; the increases never exceed what the decreases released.
