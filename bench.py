@@ -545,6 +545,8 @@ def workload_config(w):
 # Rates, fractions and the roofline of one timed run
 # ---------------------------------------------------------------------------
 FLOP_PER_CYCLE_SM = 8192   # M=256, N=128, K=16 UMMA on a CTA pair every 64 cycles (measured, sm_103a)
+FP32_FLOP_PER_CYCLE_SM = 256  # 128 fp32 FMA lanes per SM, 2 flop each: the fp32 path's (CUDA-core) peak
+SM_MAX_MHZ = 2070          # GB300's maximum SM clock, for runs too short for a clock sample
 SUSTAINED_AFTER_S = 2.0    # a timed region at least this long is compared with the sustained peak
 
 
@@ -569,10 +571,14 @@ def run_summary(w, r, peaks, src):
     long_run = r["timed_s"] >= SUSTAINED_AFTER_S
     clk = (r["clocks"] or {}).get("sm_mhz")
     clock_peak = FLOP_PER_CYCLE_SM * sm_count() * clk * 1e6 / 1e12 if clk else None
+    # The fp32 path runs on the CUDA cores: its peak is the fp32 FMA rate at
+    # the sampled clock (the maximum clock when the run was too short to sample).
+    alu_mhz = clk or SM_MAX_MHZ
+    alu_peak = FP32_FLOP_PER_CYCLE_SM * sm_count() * alu_mhz * 1e6 / 1e12
 
     def tensor_fracs(tf):
-        if w.dtype != "bf16":   # the fp32 path runs on the CUDA cores: no bf16 tensor peak applies
-            return {"tflops": tf}
+        if w.dtype != "bf16":   # no bf16 tensor peak applies
+            return {"tflops": tf, "frac_alu": tf / alu_peak}
         out = {"tflops": tf, "frac_burst": tf / burst, "frac_sustained": tf / sustained}
         if clock_peak:
             out["frac_of_clock_peak"] = tf / clock_peak
@@ -586,7 +592,7 @@ def run_summary(w, r, peaks, src):
     for name, k in r["kernels"].items():
         cname, bound, units, unit = work[name]
         rate = units * steps / (k["total_ms"] * 1e-3)
-        per_kernel[name] = dict(k, kernel=cname, bound=bound,
+        per_kernel[name] = dict(k, kernel=cname, bound="alu" if unit == "flop" and w.dtype != "bf16" else bound,
                                 **(tensor_fracs(rate / 1e12) if unit == "flop" else
                                    {"gbs": rate / 1e9, "frac_hbm": rate / 1e9 / peaks["hbm_gbs"]}))
         if name == "bwd_dq" and not ds_blocks:   # S and dP are issued again here: 3 GEMMs run, 1 is its own
@@ -607,21 +613,28 @@ def run_summary(w, r, peaks, src):
     avg_ms = k["total_ms"] / k["launches"]
     per_launch = units * steps / k["launches"]
     achieved = per_launch / (avg_ms * 1e-3) / (1e12 if unit == "flop" else 1e9)
-    if unit == "flop":
+    alu = unit == "flop" and w.dtype != "bf16"
+    if alu:
+        bound, peak = "alu", alu_peak
+        peak_source = (f"derived: {FP32_FLOP_PER_CYCLE_SM} fp32 flop/cycle/SM x {sm_count()} SMs x "
+                       f"{alu_mhz:.0f} MHz ({'sampled' if clk else 'maximum'} SM clock)")
+    elif unit == "flop":
         peak, peak_name = (sustained, "bf16_tflops_sustained") if long_run else (burst, "bf16_tflops")
     else:
         peak, peak_name = peaks["hbm_gbs"], "hbm_gbs"
+    if not alu:
+        peak_source = (f"{src} {peak_name} (timed region {r['timed_s']:.2f} s: "
+                       f"{'sustained' if long_run else 'burst'} peak)")
     traffic, traffic_how = captured_traffic(cname, w.name)
     roof = {"bound": bound, "kernel": cname, "achieved": achieved, "peak": peak,
             "unit": "TFLOP/s" if unit == "flop" else "GB/s", "frac": achieved / peak, "traffic": traffic,
             "traffic_source": traffic_how,
-            "peak_source": f"{src} {peak_name} (timed region {r['timed_s']:.2f} s: "
-                           f"{'sustained' if long_run else 'burst'} peak)",
+            "peak_source": peak_source,
             "algorithmic_per_launch": per_launch, "algorithmic_unit": unit, "avg_launch_ms": avg_ms,
             "launches": k["launches"],
             "share_of_step": k["total_ms"] / (r["ms_per_step"] * steps),
             "timing": "CUDA events recorded by the library around each launch on its stream"}
-    if unit == "flop":
+    if unit == "flop" and not alu:
         roof.update({"frac_sustained": achieved / sustained, "frac_burst": achieved / burst})
         if clock_peak:
             roof["frac_of_clock_peak"] = achieved / clock_peak
