@@ -198,18 +198,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         constexpr uint32_t idesc_s = idesc_bf16_f32(256, 128, 0, 0);  // Q (K-major) x K (K-major)
         constexpr uint32_t idesc_o = idesc_bf16_f32(256, 128, 0, 1);  // P (tmem) x V (MN-major)
+        // Descriptors are formed once per tile and stepped by constants, so
+        // that each UMMA costs the issuing thread one add.
         auto issue_s = [&](int t, int st) {
-          const uint32_t q = sQ0 + t * kTile, k = sb + kOffStage + st * kStage;
+          const uint64_t dq = sdesc_sw128(sQ0 + t * kTile, 0, 1024);
+          const uint64_t dk = sdesc_sw128(sb + kOffStage + st * kStage, 0, 1024);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma2_ss(tmem + t * 128, sdesc_sw128(q + (kk >> 2) * kHalf + (kk & 3) * 32, 0, 1024),
-                     sdesc_sw128(k + (kk >> 2) * (kHalf / 2) + (kk & 3) * 32, 0, 1024), idesc_s, kk > 0);
+            umma2_ss(tmem + t * 128, sdesc_add(dq, (kk >> 2) * kHalf + (kk & 3) * 32),
+                     sdesc_add(dk, (kk >> 2) * (kHalf / 2) + (kk & 3) * 32), idesc_s, kk > 0);
         };
         auto issue_pv = [&](int t, int st, bool acc) {
-          const uint32_t v = sb + kOffStage + st * kStage + kHalf;
+          const uint64_t dv = sdesc_sw128(sb + kOffStage + st * kStage + kHalf, kHalf, 1024);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma2_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, sdesc_sw128(v + kk * 2048, kHalf, 1024), idesc_o,
+            umma2_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, sdesc_add(dv, kk * 2048), idesc_o,
                      (acc || kk > 0) ? 1u : 0u);
         };
         bool ok = mbar_wait(bar(B_QFULL), 0, lim) && mbar_wait(bar(B_KVFULL), 0, lim);

@@ -154,6 +154,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// The descriptor of the same layout `bytes` further on (a multiple of 16):
+// the start address field holds address >> 4 in 14 bits, and shared memory
+// addresses stay below 256 KB, so adding bytes >> 4 never carries out of it.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32 accumulator.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format (1 = bf16),
 //   bit 15 A major (0 = K-major, 1 = MN-major), bit 16 B major,
