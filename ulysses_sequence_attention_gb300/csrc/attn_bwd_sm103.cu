@@ -692,25 +692,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         constexpr uint32_t id_kk = idesc_bf16_f32(256, 128, 0, 0);
         constexpr uint32_t id_tm = idesc_bf16_f32(256, 128, 0, 1);
-        const uint32_t sQ = sb + kOffQ, sDO = sb + kOffDO;
-        auto a_kmaj = [](uint32_t base, int kk) {
-          return sdesc_sw128(base + (kk >> 2) * kHalf + (kk & 3) * 32, 0, 1024);
-        };
-        auto b_kmaj64 = [](uint32_t base, int kk) {
-          return sdesc_sw128(base + (kk >> 2) * (kHalf / 2) + (kk & 3) * 32, 0, 1024);
-        };
-        auto b_mn = [](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, kHalf, 1024); };
+        // Descriptors are formed once per operand and stepped by constants,
+        // so that each UMMA costs the issuing thread one add.
+        auto kmaj = [](uint32_t base) { return sdesc_sw128(base, 0, 1024); };
+        auto a_kmaj = [](uint64_t d, int kk) { return sdesc_add(d, (kk >> 2) * kHalf + (kk & 3) * 32); };
+        auto b_kmaj64 = [](uint64_t d, int kk) { return sdesc_add(d, (kk >> 2) * (kHalf / 2) + (kk & 3) * 32); };
+        auto b_mn = [](uint64_t d, int kk) { return sdesc_add(d, kk * 2048); };
         auto issue_s = [&](int jj) {
-          const uint32_t sk = sb + kOffStage + (jj % NK) * kStage;
+          const uint64_t dq = kmaj(sb + kOffQ), dk = kmaj(sb + kOffStage + (jj % NK) * kStage);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) umma2_ss(tmem + 0, a_kmaj(sQ, kk), b_kmaj64(sk, kk), id_kk, kk > 0);
+          for (int kk = 0; kk < 8; ++kk) umma2_ss(tmem + 0, a_kmaj(dq, kk), b_kmaj64(dk, kk), id_kk, kk > 0);
         };
         // dP of tile jj into buffer jj&1; its commit also covers S of the tile.
         auto issue_dp = [&](int jj) {
-          const uint32_t sk = sb + kOffStage + (jj % NK) * kStage;
+          const uint64_t ddo = kmaj(sb + kOffDO), dv = kmaj(sb + kOffStage + (jj % NK) * kStage + kHalf);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma2_ss(tmem + 128 + 128 * (jj & 1), a_kmaj(sDO, kk), b_kmaj64(sk + kHalf, kk), id_kk, kk > 0);
+            umma2_ss(tmem + 128 + 128 * (jj & 1), a_kmaj(ddo, kk), b_kmaj64(dv, kk), id_kk, kk > 0);
           umma2_commit_both(bar(B_DP));
         };
         bool ok = mbar_wait(bar(B_QO), 0, lim) && mbar_wait(bar(B_KFULL), 0, lim);
@@ -737,11 +735,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           if (!mbar_wait(bar(B_DS), jj & 1, lim)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t sk = sb + kOffStage + st * kStage;
+          const uint64_t dkh = sdesc_sw128(sb + kOffStage + st * kStage + 2 * kHalf, kHalf, 1024);
           const uint32_t ds = tmem + 128 + 128 * (jj & 1);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)  // dQ += dS K; key half kk/4 of dS at +64 (kk/4)
-            umma2_ts(tmem + 384, ds + (kk >> 2) * 64 + (kk & 3) * 8, b_mn(sk + 2 * kHalf, kk), id_tm,
+            umma2_ts(tmem + 384, ds + (kk >> 2) * 64 + (kk & 3) * 8, b_mn(dkh, kk), id_tm,
                      (jj > 0 || kk > 0) ? 1u : 0u);
           umma2_commit_both(bar(B_KEMPTY + st));  // the key stage is free once dQ has read it
         }
